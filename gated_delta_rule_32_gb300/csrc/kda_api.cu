@@ -1,0 +1,240 @@
+// kda_api.cu -- the C ABI of libkda.so: argument checks, path selection,
+// the end-to-end host-buffer call.  Every step of the forward runs in the
+// library's own kernels; there is no CPU fallback.
+#include <stdio.h>
+#include <string.h>
+
+#include "kda_common.cuh"
+
+namespace {
+
+bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+struct Sizes {
+  size_t qk, v, beta, state, cu;  // bytes
+};
+
+Sizes sizes_of(int B, int T, int H, int dk, int dv, int esz, int packed) {
+  Sizes s;
+  const size_t rows = packed ? 1 : (size_t)B;
+  s.qk = rows * (size_t)T * H * dk * esz;
+  s.v = rows * (size_t)T * H * dv * esz;
+  s.beta = rows * (size_t)T * H * esz;
+  s.state = (size_t)B * H * dk * dv * sizeof(float);
+  s.cu = packed ? (size_t)(B + 1) * sizeof(int32_t) : 0;
+  return s;
+}
+
+kda_status check_args(const void* q, const void* k, const void* v, const void* g,
+                      const void* beta, const float* s0, const void* out, const float* s1,
+                      int B, int T, int H, int dk, int dv, const int32_t* cu, int dtype,
+                      int chunk_size, int algo) {
+  if (B < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_ARG;
+  // with no tokens nothing is read or written but the states
+  if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_INVALID_ARG;
+  if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+  if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+  if (chunk_size != 0 && chunk_size != 16 && chunk_size != 64) return KDA_ERR_UNSUPPORTED;
+  if (algo < KDA_ALGO_AUTO || algo > KDA_ALGO_TC) return KDA_ERR_INVALID_ARG;
+  const int esz = dtype == KDA_F32 ? 4 : 2;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
+      !aligned(out, 16) || !aligned(beta, esz))
+    return KDA_ERR_MISALIGNED;
+  if ((s0 && !aligned(s0, 16)) || (s1 && !aligned(s1, 16)) || (cu && !aligned(cu, 4)))
+    return KDA_ERR_MISALIGNED;
+  Sizes s = sizes_of(B, T, H, dk, dv, esz, cu != nullptr);
+  if (overlap(out, s.v, q, s.qk) || overlap(out, s.v, k, s.qk) || overlap(out, s.v, g, s.qk) ||
+      overlap(out, s.v, v, s.v) || overlap(out, s.v, beta, s.beta) ||
+      overlap(out, s.v, s0, s.state) || overlap(out, s.v, s1, s.state))
+    return KDA_ERR_INVALID_ARG;
+  if (s1 && s0 != s1 &&
+      (overlap(s1, s.state, q, s.qk) || overlap(s1, s.state, k, s.qk) ||
+       overlap(s1, s.state, g, s.qk) || overlap(s1, s.state, v, s.v) ||
+       overlap(s1, s.state, s0, s.state)))
+    return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+bool use_tc(int dtype, int dk, int dv, int chunk_size, int algo) {
+  if (algo == KDA_ALGO_SIMT) return false;
+  if (dtype != KDA_BF16 || chunk_size == 16) return false;
+  return kda_tc_supported(dk, dv);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: null pointer, bad size or aliasing";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: dk/dv/chunk/dtype not supported";
+    case KDA_ERR_MISALIGNED: return "KDA_ERR_MISALIGNED: pointer alignment rule broken";
+    case KDA_ERR_BAD_SEQLENS: return "KDA_ERR_BAD_SEQLENS: cu_seqlens malformed";
+    case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: bounded on-chip wait gave up";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
+    case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace too small";
+  }
+  return "KDA_ERR_UNKNOWN";
+}
+
+const char* kda_build_info(void) {
+  return "libkda: KDA chunked forward, sm_103a (tcgen05/TMEM/TMA fused path + fp32 CUDA-core path)";
+}
+
+int kda_resolve_algo(int dtype, int dk, int dv, int chunk_size, int algo) {
+  if (dtype != KDA_BF16 && dtype != KDA_F32) return -1;
+  if (!dim_ok(dk) || !dim_ok(dv)) return -1;
+  if (chunk_size != 0 && chunk_size != 16 && chunk_size != 64) return -1;
+  if (algo < KDA_ALGO_AUTO || algo > KDA_ALGO_TC) return -1;
+  const bool tc = use_tc(dtype, dk, dv, chunk_size, algo);
+  if (algo == KDA_ALGO_TC && !tc) return -1;
+  return tc ? KDA_ALGO_TC : KDA_ALGO_SIMT;
+}
+
+size_t kda_workspace_bytes(int N, int T, int H, int dk, int dv, int dtype, int chunk_size,
+                           int algo, int packed) {
+  (void)N; (void)T; (void)H; (void)dk; (void)dv; (void)dtype; (void)chunk_size; (void)algo;
+  (void)packed;
+  return 0;
+}
+
+kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, const void* g_logit,
+                            const void* beta, const float* init_state, void* out,
+                            float* final_state, int B, int T, int H, int dk, int dv,
+                            const int32_t* cu_seqlens, kda_dtype dtype, int chunk_size,
+                            float scale, int algo, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, kda_stream_t stream_) {
+  kda_status st = check_args(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk,
+                             dv, cu_seqlens, dtype, chunk_size, algo);
+  if (st != KDA_OK) return st;
+  const size_t need = kda_workspace_bytes(B, T, H, dk, dv, dtype, chunk_size, algo,
+                                          cu_seqlens != nullptr);
+  if (need > 0 && workspace && workspace_bytes < need) return KDA_ERR_WORKSPACE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), stream) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  kda::FwdParams p;
+  p.q = q; p.k = k; p.v = v; p.g = g_logit; p.beta = beta;
+  p.init_state = init_state; p.out = out; p.final_state = final_state;
+  p.cu_seqlens = cu_seqlens; p.dev_status = dev_status;
+  p.N = B; p.T = T; p.H = H; p.dk = dk; p.dv = dv; p.scale = scale;
+  if (algo == KDA_ALGO_TC && !use_tc(dtype, dk, dv, chunk_size, algo))
+    return KDA_ERR_UNSUPPORTED;
+  if (use_tc(dtype, dk, dv, chunk_size, algo)) return kda_launch_tc(p, stream);
+  return kda_launch_simt(p, dtype, stream);
+}
+
+kda_status kda_chunk_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const uint16_t* g_logit, const uint16_t* beta,
+                         const float* init_state, uint16_t* out, float* final_state,
+                         int B, int T, int H, int dk, int dv, const int32_t* cu_seqlens,
+                         kda_stream_t stream) {
+  return kda_chunk_fwd_ex(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk,
+                          dv, cu_seqlens, KDA_BF16, 0, 1.0f, KDA_ALGO_AUTO, nullptr, 0,
+                          nullptr, stream);
+}
+
+kda_status kda_chunk_fwd_f32(const float* q, const float* k, const float* v,
+                             const float* g_logit, const float* beta,
+                             const float* init_state, float* out, float* final_state,
+                             int B, int T, int H, int dk, int dv, const int32_t* cu_seqlens,
+                             kda_stream_t stream) {
+  return kda_chunk_fwd_ex(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk,
+                          dv, cu_seqlens, KDA_F32, 0, 1.0f, KDA_ALGO_AUTO, nullptr, 0,
+                          nullptr, stream);
+}
+
+static size_t round_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t kda_host_staging_bytes(int B, int T, int H, int dk, int dv, int dtype, int has_init,
+                              int has_final, int packed) {
+  if (B < 1 || T < 0 || H < 1 || dk < 1 || dv < 1) return 0;
+  const int esz = dtype == KDA_F32 ? 4 : 2;
+  Sizes s = sizes_of(B, T, H, dk, dv, esz, packed);
+  size_t tot = 3 * round_up(s.qk) + 2 * round_up(s.v) + round_up(s.beta);
+  if (has_init) tot += round_up(s.state);
+  if (has_final) tot += round_up(s.state);
+  tot += round_up(s.cu) + 256;  // cu_seqlens + device status word
+  return tot;
+}
+
+kda_status kda_chunk_fwd_host(const void* q, const void* k, const void* v, const void* g_logit,
+                              const void* beta, const float* init_state, void* out,
+                              float* final_state, int B, int T, int H, int dk, int dv,
+                              const int32_t* cu_seqlens, kda_dtype dtype, float scale,
+                              void* dev_buffer, size_t dev_buffer_bytes, kda_stream_t stream_) {
+  if (B < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_ARG;
+  if (T > 0 && (!q || !k || !v || !g_logit || !beta || !out)) return KDA_ERR_INVALID_ARG;
+  if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
+  if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const int packed = cu_seqlens != nullptr;
+  if (packed) {  // host-visible offsets: check them before any copy
+    if (cu_seqlens[0] != 0 || cu_seqlens[B] != T) return KDA_ERR_BAD_SEQLENS;
+    for (int n = 0; n < B; ++n)
+      if (cu_seqlens[n + 1] < cu_seqlens[n]) return KDA_ERR_BAD_SEQLENS;
+  }
+  const int esz = dtype == KDA_F32 ? 4 : 2;
+  Sizes s = sizes_of(B, T, H, dk, dv, esz, packed);
+  const size_t need = kda_host_staging_bytes(B, T, H, dk, dv, dtype, init_state != nullptr,
+                                             final_state != nullptr, packed);
+  char* base = static_cast<char*>(dev_buffer);
+  bool owned = false;
+  if (!base) {
+    if (cudaMallocAsync((void**)&base, need, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    owned = true;
+  } else if (dev_buffer_bytes < need) {
+    return KDA_ERR_WORKSPACE;
+  }
+  size_t off = 0;
+  auto take = [&](size_t n) { char* p = base + off; off += round_up(n); return p; };
+  char *dq = take(s.qk), *dk_ = take(s.qk), *dg = take(s.qk), *dv_ = take(s.v),
+       *dout = take(s.v), *db = take(s.beta);
+  float* ds0 = init_state ? (float*)take(s.state) : nullptr;
+  float* ds1 = final_state ? (float*)take(s.state) : nullptr;
+  int32_t* dcu = packed ? (int32_t*)take(s.cu) : nullptr;
+  int32_t* dstat = (int32_t*)take(sizeof(int32_t));
+  kda_status st = KDA_OK;
+  int32_t hstat = 0;
+  bool ok = true;
+  ok = ok && cudaMemcpyAsync(dq, q, s.qk, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(dk_, k, s.qk, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(dg, g_logit, s.qk, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(dv_, v, s.v, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+  ok = ok && cudaMemcpyAsync(db, beta, s.beta, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+  if (ds0)
+    ok = ok &&
+         cudaMemcpyAsync(ds0, init_state, s.state, cudaMemcpyHostToDevice, stream) == cudaSuccess;
+  if (dcu)
+    ok = ok && cudaMemcpyAsync(dcu, cu_seqlens, s.cu, cudaMemcpyHostToDevice, stream) ==
+                   cudaSuccess;
+  if (!ok) st = KDA_ERR_CUDA;
+  if (st == KDA_OK)
+    st = kda_chunk_fwd_ex(dq, dk_, dv_, dg, db, ds0, dout, ds1, B, T, H, dk, dv, dcu, dtype, 0,
+                          scale, KDA_ALGO_AUTO, nullptr, 0, dstat, stream_);
+  if (st == KDA_OK) {
+    ok = cudaMemcpyAsync(out, dout, s.v, cudaMemcpyDeviceToHost, stream) == cudaSuccess;
+    if (ds1)
+      ok = ok && cudaMemcpyAsync(final_state, ds1, s.state, cudaMemcpyDeviceToHost, stream) ==
+                     cudaSuccess;
+    ok = ok &&
+         cudaMemcpyAsync(&hstat, dstat, sizeof(int32_t), cudaMemcpyDeviceToHost, stream) ==
+             cudaSuccess;
+    if (!ok) st = KDA_ERR_CUDA;
+  }
+  if (owned) cudaFreeAsync(base, stream);
+  if (cudaStreamSynchronize(stream) != cudaSuccess && st == KDA_OK) st = KDA_ERR_CUDA;
+  if (st == KDA_OK && hstat != 0) st = (kda_status)hstat;
+  return st;
+}
+
+}  // extern "C"

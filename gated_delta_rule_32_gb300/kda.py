@@ -1,0 +1,189 @@
+"""ctypes binding of libkda.so (include/kda.h), argument marshalling only.
+
+The functions keep the C names.  Tensor arguments may be torch tensors
+(their data_ptr() is passed) or raw integer addresses; None is NULL.  Every
+step of the forward runs in the library's kernels: if the library is not
+built, or there is no GPU, calls fail loudly; nothing here computes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "kda.h")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_MISALIGNED = 3
+KDA_ERR_BAD_SEQLENS = 4
+KDA_ERR_TIMEOUT = 5
+KDA_ERR_CUDA = 6
+KDA_ERR_WORKSPACE = 7
+KDA_BF16 = 0
+KDA_F32 = 1
+KDA_ALGO_AUTO = 0
+KDA_ALGO_SIMT = 1
+KDA_ALGO_TC = 2
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_SIGS = {
+    "kda_status_string": (ctypes.c_char_p, [_i]),
+    "kda_build_info": (ctypes.c_char_p, []),
+    "kda_resolve_algo": (_i, [_i] * 5),
+    "kda_chunk_fwd": (_i, [_vp] * 8 + [_i] * 5 + [_vp, _vp]),
+    "kda_chunk_fwd_f32": (_i, [_vp] * 8 + [_i] * 5 + [_vp, _vp]),
+    "kda_chunk_fwd_ex": (_i, [_vp] * 8 + [_i] * 5 + [_vp, _i, _i, ctypes.c_float, _i, _vp,
+                                                   ctypes.c_size_t, _vp, _vp]),
+    "kda_workspace_bytes": (ctypes.c_size_t, [_i] * 9),
+    "kda_chunk_fwd_host": (_i, [_vp] * 8 + [_i] * 5 + [_vp, _i, ctypes.c_float, _vp,
+                                                   ctypes.c_size_t, _vp]),
+    "kda_host_staging_bytes": (ctypes.c_size_t, [_i] * 9),
+    "kda_debug_intra": (_i, [_vp] * 5 + [_i] * 5 + [_vp, _i, _i] + [_vp] * 6 + [_vp]),
+}
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__("%s failed: %s" % (fn, status_string(code) if _lib else code))
+
+
+def load(path: str = LIB_PATH):
+    """Load libkda.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    "libkda.so not found at %s: build it with "
+                    "`python -m gated_delta_rule_32_gb300.build` (needs nvcc)" % path)
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in _SIGS.items():
+                f = getattr(lib, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def header_functions(header: str = HEADER):
+    """Names of the functions include/kda.h declares."""
+    txt = open(header).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(kda_[a-z_0-9]+)\s*\(",
+                                 txt, flags=re.M)))
+
+
+def _p(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def status_string(code: int) -> str:
+    return load().kda_status_string(int(code)).decode()
+
+
+def kda_build_info() -> str:
+    return load().kda_build_info().decode()
+
+
+def kda_resolve_algo(dtype=KDA_BF16, dk=128, dv=128, chunk_size=0, algo=KDA_ALGO_AUTO) -> int:
+    return load().kda_resolve_algo(dtype, dk, dv, chunk_size, algo)
+
+
+def kda_chunk_fwd(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk, dv,
+                  cu_seqlens=None, stream=None) -> int:
+    return load().kda_chunk_fwd(_p(q), _p(k), _p(v), _p(g_logit), _p(beta), _p(init_state),
+                                _p(out), _p(final_state), B, T, H, dk, dv, _p(cu_seqlens),
+                                _stream(stream))
+
+
+def kda_chunk_fwd_f32(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk, dv,
+                      cu_seqlens=None, stream=None) -> int:
+    return load().kda_chunk_fwd_f32(_p(q), _p(k), _p(v), _p(g_logit), _p(beta),
+                                    _p(init_state), _p(out), _p(final_state), B, T, H, dk, dv,
+                                    _p(cu_seqlens), _stream(stream))
+
+
+def kda_chunk_fwd_ex(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk, dv,
+                     cu_seqlens=None, dtype=KDA_BF16, chunk_size=0, scale=1.0,
+                     algo=KDA_ALGO_AUTO, workspace=None, workspace_bytes=0, dev_status=None,
+                     stream=None) -> int:
+    return load().kda_chunk_fwd_ex(_p(q), _p(k), _p(v), _p(g_logit), _p(beta), _p(init_state),
+                                   _p(out), _p(final_state), B, T, H, dk, dv, _p(cu_seqlens),
+                                   dtype, chunk_size, float(scale), algo, _p(workspace),
+                                   workspace_bytes, _p(dev_status), _stream(stream))
+
+
+def kda_workspace_bytes(N, T, H, dk, dv, dtype=KDA_BF16, chunk_size=0, algo=KDA_ALGO_AUTO,
+                        packed=0) -> int:
+    return load().kda_workspace_bytes(N, T, H, dk, dv, dtype, chunk_size, algo, int(packed))
+
+
+def kda_chunk_fwd_host(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk, dv,
+                       cu_seqlens=None, dtype=KDA_BF16, scale=1.0, dev_buffer=None,
+                       dev_buffer_bytes=0, stream=None) -> int:
+    return load().kda_chunk_fwd_host(_p(q), _p(k), _p(v), _p(g_logit), _p(beta),
+                                     _p(init_state), _p(out), _p(final_state), B, T, H, dk, dv,
+                                     _p(cu_seqlens), dtype, float(scale), _p(dev_buffer),
+                                     dev_buffer_bytes, _stream(stream))
+
+
+def kda_host_staging_bytes(B, T, H, dk, dv, dtype=KDA_BF16, has_init=0, has_final=0,
+                           packed=0) -> int:
+    return load().kda_host_staging_bytes(B, T, H, dk, dv, dtype, int(has_init),
+                                         int(has_final), int(packed))
+
+
+def kda_debug_intra(q, k, v, g_logit, beta, B, T, H, dk, dv, cu_seqlens, n, h, gam=None,
+                    aqk=None, akk=None, tinv=None, w=None, u=None, stream=None) -> int:
+    return load().kda_debug_intra(_p(q), _p(k), _p(v), _p(g_logit), _p(beta), B, T, H, dk, dv,
+                                  _p(cu_seqlens), n, h, _p(gam), _p(aqk), _p(akk), _p(tinv),
+                                  _p(w), _p(u), _stream(stream))
+
+
+def forward(q, k, v, g_logit, beta, init_state=None, cu_seqlens=None, scale=1.0,
+            output_final_state=True, chunk_size=0, algo=KDA_ALGO_AUTO, dev_status=None,
+            stream=None):
+    """Allocate the outputs and call kda_chunk_fwd_ex on the current stream.
+
+    q, k, g_logit [B,T,H,dk], v [B,T,H,dv], beta [B,T,H] CUDA tensors of one
+    dtype (bfloat16 or float32); init_state [N,H,dk,dv] fp32 or None;
+    cu_seqlens int32 [N+1] CUDA tensor or None.  Returns (out, final_state).
+    """
+    import torch
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    dtype = {torch.bfloat16: KDA_BF16, torch.float32: KDA_F32}[q.dtype]
+    out = torch.empty(B, T, H, dv, dtype=q.dtype, device=q.device)
+    fs = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device) \
+        if output_final_state else None
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = kda_chunk_fwd_ex(q, k, v, g_logit, beta, init_state, out, fs, N, T, H, dk, dv,
+                          cu_seqlens, dtype, chunk_size, scale, algo, None, 0, dev_status,
+                          stream)
+    if rc != KDA_OK:
+        raise KdaError("kda_chunk_fwd_ex", rc)
+    return out, fs

@@ -1,0 +1,182 @@
+/*
+ * kda.h -- C ABI of libkda.so: the chunkwise-parallel forward of Kimi Delta
+ * Attention (KDA) on one GB300 (sm_103a).
+ *
+ * The operation.  For every (sequence n, head h), with a state S of dk x dv
+ * (row i = key channel, column j = value channel):
+ *
+ *   a_t = max(-softplus(g_logit_t), -5)                (per key channel)
+ *   S_t = (I - beta_t k_t k_t^T) Diag(exp(a_t)) S_{t-1} + beta_t k_t v_t^T
+ *   o_t = S_t^T (scale * q_t)
+ *
+ *  - gated delta rule with a diagonal, per-channel decay, computable in a
+ *    chunk-parallel form; decay logits through a negative softplus:
+ *    Kimi K3 walkthrough (Towards AI, M. Zhao), section "Kimi Delta
+ *    Attention (KDA)";
+ *  - floor of -5 on the per-step log-decay (at least ~0.67% kept), which
+ *    holds a 16-token tile's cumulative log-decay in [-80, 0] so that every
+ *    intra-chunk tile, diagonal ones included, is one dense BF16 product:
+ *    Kimi K3 architecture (orkas.ai), section "A lower bound that erased a
+ *    GPU code path";
+ *  - fixed-size recurrent state that does not grow with the sequence:
+ *    same page, section "Sequence"; the state as checkpoint/hand-over
+ *    quantity: section "The cost is paid in the serving stack".
+ * beta is the already-squashed write strength (e.g. a sigmoid output).
+ * scale multiplies q (1.0 = none).
+ *
+ * Layouts (row-major, contiguous, no padding):
+ *   q, k, g_logit    [B, T, H, dk]      v, out    [B, T, H, dv]
+ *   beta             [B, T, H]
+ *   init_state, final_state   [N, H, dk, dv] fp32 (N = B when dense)
+ * Packed variable-length batches: cu_seqlens (int32, DEVICE memory, N + 1
+ * entries, cu_seqlens[0] = 0, non-decreasing, cu_seqlens[N] = T); the
+ * tensors are then [1, T, H, .] and the B argument carries N.  Chunks and
+ * 16-token tiles restart at every sequence start.
+ *
+ * Ownership: the caller owns every buffer; the library keeps no pointer
+ * after a call returns.  Device pointers must come from the current device.
+ * init_state may equal final_state (in-place resume); out must not alias
+ * any input.  Either state pointer may be NULL (zero initial state / final
+ * state not wanted).
+ *
+ * Asynchrony: the device entry points enqueue work on `stream` and return;
+ * outputs are valid once the stream has reached that point.  Problems the
+ * host can see (NULL required pointers, sizes, alignment) return an error
+ * before anything is enqueued and nothing is written.  Problems only the
+ * device can see (malformed cu_seqlens, a wait that timed out) are written
+ * to `dev_status` (kda_chunk_fwd_ex) as a kda_status value; the affected
+ * outputs are then unspecified, and no access ever leaves the buffers the
+ * arguments describe.
+ *
+ * Alignment: q, k, v, g_logit, out 16-byte aligned; beta 2-byte (bf16) or
+ * 4-byte (fp32); states 16-byte aligned.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* kda_stream_t;
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,  /* NULL required pointer, non-positive size, out aliasing */
+  KDA_ERR_UNSUPPORTED = 2,  /* dk / dv / chunk / dtype combination not built */
+  KDA_ERR_MISALIGNED = 3,   /* a pointer breaks the alignment rule above */
+  KDA_ERR_BAD_SEQLENS = 4,  /* cu_seqlens not 0 .. T non-decreasing (device-detected) */
+  KDA_ERR_TIMEOUT = 5,      /* a bounded on-chip wait gave up (device-detected) */
+  KDA_ERR_CUDA = 6,         /* a CUDA runtime call failed */
+  KDA_ERR_WORKSPACE = 7     /* workspace given but smaller than kda_workspace_bytes() */
+} kda_status;
+
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
+
+/* Implementation choice for kda_chunk_fwd_ex (the result is the same
+ * function of the inputs up to rounding). */
+typedef enum {
+  KDA_ALGO_AUTO = 0,  /* tensor-core path where built, else CUDA-core path */
+  KDA_ALGO_SIMT = 1,  /* fp32 CUDA-core chunked path (16-token chunks) */
+  KDA_ALGO_TC = 2     /* tcgen05/TMEM/TMA fused path (bf16, dk = dv = 128) */
+} kda_algo;
+
+/* Human-readable name of a status code (static storage). */
+const char* kda_status_string(kda_status s);
+
+/*
+ * kda_chunk_fwd -- forward for BF16 inputs (values stored as bf16 bit
+ * patterns, uint16_t), fp32 states, bf16 output rounded to nearest even.
+ * dk, dv in {16, 32, 64, 128}; B, H >= 1; T >= 0.  Device pointers.
+ */
+kda_status kda_chunk_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const uint16_t* g_logit, const uint16_t* beta,
+                         const float* init_state, uint16_t* out, float* final_state,
+                         int B, int T, int H, int dk, int dv, const int32_t* cu_seqlens,
+                         kda_stream_t stream);
+
+/* Same, fp32 inputs and output (CUDA-core path, fp32 arithmetic). */
+kda_status kda_chunk_fwd_f32(const float* q, const float* k, const float* v,
+                             const float* g_logit, const float* beta,
+                             const float* init_state, float* out, float* final_state,
+                             int B, int T, int H, int dk, int dv, const int32_t* cu_seqlens,
+                             kda_stream_t stream);
+
+/*
+ * kda_chunk_fwd_ex -- the general entry point.
+ *   dtype       KDA_BF16 or KDA_F32 (q, k, v, g_logit, beta, out).
+ *   chunk_size  0 (implementation's choice), 16 or 64; no effect on the
+ *               result beyond rounding.  16 selects the CUDA-core path.
+ *   scale       multiplies q.
+ *   algo        kda_algo.
+ *   workspace   device scratch of at least kda_workspace_bytes() bytes, or
+ *               NULL: the library then takes it from the stream-ordered
+ *               allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *   dev_status  NULL or one device int32; set to KDA_OK at the start of the
+ *               work and to a device-detected error if one occurs.
+ */
+kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, const void* g_logit,
+                            const void* beta, const float* init_state, void* out,
+                            float* final_state, int B, int T, int H, int dk, int dv,
+                            const int32_t* cu_seqlens, kda_dtype dtype, int chunk_size,
+                            float scale, int algo, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, kda_stream_t stream);
+
+/* Device scratch bytes kda_chunk_fwd_ex needs for these sizes (0 = none).
+ * N = number of sequences (B, or the cu_seqlens count when packed). */
+size_t kda_workspace_bytes(int N, int T, int H, int dk, int dv, int dtype, int chunk_size,
+                           int algo, int packed);
+
+/*
+ * kda_chunk_fwd_host -- end-to-end call on HOST buffers (pinned memory
+ * recommended): copies the inputs (and cu_seqlens) to the device, runs the
+ * forward, copies out and final_state back and synchronises `stream`
+ * before returning.  Same layouts and rules as kda_chunk_fwd_ex; every
+ * pointer here is a host pointer.  dev_buffer: device memory of at least
+ * kda_host_staging_bytes() bytes, or NULL (then taken from and returned to
+ * the stream-ordered allocator).  The device status is read back and
+ * returned as the call's result.
+ */
+kda_status kda_chunk_fwd_host(const void* q, const void* k, const void* v, const void* g_logit,
+                              const void* beta, const float* init_state, void* out,
+                              float* final_state, int B, int T, int H, int dk, int dv,
+                              const int32_t* cu_seqlens, kda_dtype dtype, float scale,
+                              void* dev_buffer, size_t dev_buffer_bytes, kda_stream_t stream);
+
+/* Device bytes kda_chunk_fwd_host stages through for these sizes. */
+size_t kda_host_staging_bytes(int B, int T, int H, int dk, int dv, int dtype, int has_init,
+                              int has_final, int packed);
+
+/*
+ * Test hooks (not part of the hot path): the intra-chunk steps of the
+ * tensor-core path for one (sequence n, head h), every chunk, written to
+ * fp32 device buffers laid out [n_chunks, 64, .]:
+ *   gam  [., 64, dk]  cumulative log-decay from the chunk start
+ *   aqk  [., 64, 64]  A_qk incl. diagonal (upper part zero)
+ *   akk  [., 64, 64]  beta-weighted A_kk, strictly lower
+ *   tinv [., 64, 64]  (I + A_kk)^{-1}
+ *   w    [., 64, dk], u [., 64, dv]
+ * Inputs as kda_chunk_fwd (bf16, dense or packed).  Any output may be NULL.
+ */
+kda_status kda_debug_intra(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const uint16_t* g_logit, const uint16_t* beta, int B, int T, int H,
+                           int dk, int dv, const int32_t* cu_seqlens, int n, int h,
+                           float* gam, float* aqk, float* akk, float* tinv, float* w,
+                           float* u, kda_stream_t stream);
+
+/* The path kda_chunk_fwd_ex would take for these arguments: KDA_ALGO_SIMT
+ * or KDA_ALGO_TC, or -1 if the combination is unsupported. */
+int kda_resolve_algo(int dtype, int dk, int dv, int chunk_size, int algo);
+
+/* Library build identification (static string). */
+const char* kda_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -21,7 +21,9 @@ materialising the whole batch.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
 import dataclasses
+import os
 from typing import Optional
 
 import torch
@@ -156,19 +158,29 @@ def make_inputs(w: Workload, device="cpu"):
     beta = torch.empty(B, T, H, dtype=dt)
     N = w.n_seqs()
     s0 = torch.zeros(N, H, w.dk, w.dv) if w.s0_std > 0 else None
-    for b in range(B):
-        for h in range(H):
-            u = make_unit(w, b, h)
-            q[b, :, h] = u["q"].to(dt)
-            k[b, :, h] = u["k"].to(dt)
-            v[b, :, h] = u["v"].to(dt)
-            beta[b, :, h] = u["beta"].to(dt)
-            gt[b, :, h] = u["g"].to(dt)
-            if s0 is not None:
-                if w.varlen:
-                    s0[:, h] = u["s0"]
-                else:
-                    s0[b, h] = u["s0"][0]
+    def fill(bh):
+        b, h = bh
+        u = make_unit(w, b, h)
+        q[b, :, h] = u["q"].to(dt)
+        k[b, :, h] = u["k"].to(dt)
+        v[b, :, h] = u["v"].to(dt)
+        beta[b, :, h] = u["beta"].to(dt)
+        gt[b, :, h] = u["g"].to(dt)
+        if s0 is not None:
+            if w.varlen:
+                s0[:, h] = u["s0"]
+            else:
+                s0[b, h] = u["s0"][0]
+
+    units = [(b, h) for b in range(B) for h in range(H)]
+    # units write disjoint slices; torch kernels release the GIL
+    workers = max(1, min(len(units), os.cpu_count() or 1, 32))
+    if workers == 1 or B * T * H < (1 << 16):
+        for u in units:
+            fill(u)
+    else:
+        with cf.ThreadPoolExecutor(workers) as ex:
+            list(ex.map(fill, units))
     cu = None
     if w.varlen:
         lens = w.seqlens()

@@ -1,0 +1,98 @@
+"""The C-ABI library: builds, loads, exports every declared symbol, and
+rejects bad host-visible arguments before touching the GPU.  CPU only."""
+import ctypes
+
+import pytest
+
+import gated_delta_rule_32_gb300 as pkg
+from gated_delta_rule_32_gb300 import kda
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_32_gb300 import build
+    build.build()
+    return kda.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = kda.header_functions()
+    assert len(names) >= 9
+    raw = ctypes.CDLL(kda.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = kda.status_string(code)
+        assert s.startswith("KDA_")
+    assert kda.status_string(99) == "KDA_ERR_UNKNOWN"
+    assert "sm_103a" in kda.kda_build_info()
+
+
+A = 1 << 20   # fake, 16-byte aligned addresses: never dereferenced on the host
+
+
+def _call(**over):
+    args = dict(q=A, k=2 * A, v=3 * A, g_logit=4 * A, beta=5 * A, init_state=None,
+                out=6 * A, final_state=None, B=1, T=64, H=1, dk=128, dv=128)
+    args.update(over)
+    return kda.kda_chunk_fwd_ex(**args)
+
+
+def test_rejects_null_pointers(lib):
+    for name in ("q", "k", "v", "g_logit", "beta", "out"):
+        assert _call(**{name: None}) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_rejects_sizes(lib):
+    assert _call(B=0) == kda.KDA_ERR_INVALID_ARG
+    assert _call(H=0) == kda.KDA_ERR_INVALID_ARG
+    assert _call(T=-1) == kda.KDA_ERR_INVALID_ARG
+    assert _call(dk=48) == kda.KDA_ERR_UNSUPPORTED
+    assert _call(dv=256) == kda.KDA_ERR_UNSUPPORTED
+    assert _call(chunk_size=32) == kda.KDA_ERR_UNSUPPORTED
+    assert _call(dtype=7) == kda.KDA_ERR_UNSUPPORTED
+    assert _call(algo=9) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_rejects_misaligned(lib):
+    assert _call(q=A + 8) == kda.KDA_ERR_MISALIGNED
+    assert _call(out=6 * A + 2) == kda.KDA_ERR_MISALIGNED
+    assert _call(beta=5 * A + 1) == kda.KDA_ERR_MISALIGNED
+    assert _call(init_state=7 * A + 4) == kda.KDA_ERR_MISALIGNED
+
+
+def test_rejects_aliasing(lib):
+    assert _call(out=A) == kda.KDA_ERR_INVALID_ARG          # out == q
+    assert _call(out=3 * A + 64) == kda.KDA_ERR_INVALID_ARG  # out overlaps v
+    assert _call(final_state=2 * A) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_host_entry_rejects_bad_seqlens(lib):
+    import numpy as np
+    cu = np.array([0, 10, 5, 64], dtype=np.int32)      # decreasing
+    rc = kda.kda_chunk_fwd_host(A, 2 * A, 3 * A, 4 * A, 5 * A, None, 6 * A, None, 3, 64, 1,
+                                128, 128, cu.ctypes.data)
+    assert rc == kda.KDA_ERR_BAD_SEQLENS
+    cu = np.array([0, 10, 60], dtype=np.int32)          # does not end at T
+    rc = kda.kda_chunk_fwd_host(A, 2 * A, 3 * A, 4 * A, 5 * A, None, 6 * A, None, 2, 64, 1,
+                                128, 128, cu.ctypes.data)
+    assert rc == kda.KDA_ERR_BAD_SEQLENS
+
+
+def test_staging_bytes(lib):
+    n = kda.kda_host_staging_bytes(2, 100, 3, 128, 64, kda.KDA_BF16, 1, 1, 0)
+    qk = 2 * 100 * 3 * 128 * 2
+    assert n >= 3 * qk + 2 * 2 * 100 * 3 * 64 * 2 + 2 * 2 * 3 * 128 * 64 * 4
+
+
+def test_package_fails_loudly_without_library(tmp_path):
+    saved = kda._lib
+    try:
+        kda._lib = None
+        with pytest.raises(RuntimeError, match="libkda.so not found"):
+            kda.load(str(tmp_path / "missing.so"))
+    finally:
+        kda._lib = saved
