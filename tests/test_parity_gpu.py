@@ -107,7 +107,10 @@ def test_degenerate_gates(algo, case):
     elif case == "alpha_one":
         x["g"] = torch.full_like(x["g"], -200.0)
     elif case == "beta_zero":
+        # beta = 0 leaves only the decay of S0; keep it mild so the exact
+        # final state stays far above fp32 underflow
         x["beta"] = torch.zeros_like(x["beta"])
+        x["g"] = torch.full_like(x["g"], -4.0)
     else:
         x["beta"] = torch.ones_like(x["beta"])
     check(x, torch.bfloat16, algo)
