@@ -47,6 +47,7 @@ _SIGS = {
     "kda_chunk_fwd_host": (_i, [_vp] * 8 + [_i] * 5 + [_vp, _i, ctypes.c_float, _vp,
                                                    ctypes.c_size_t, _vp]),
     "kda_host_staging_bytes": (ctypes.c_size_t, [_i] * 9),
+    "kda_debug_umma": (_i, [_vp] * 3 + [_i] * 6 + [_vp, _vp]),
     "kda_debug_intra": (_i, [_vp] * 5 + [_i] * 5 + [_vp, _i, _i] + [_vp] * 6 + [_vp]),
 }
 
@@ -160,6 +161,12 @@ def kda_debug_intra(q, k, v, g_logit, beta, B, T, H, dk, dv, cu_seqlens, n, h, g
     return load().kda_debug_intra(_p(q), _p(k), _p(v), _p(g_logit), _p(beta), B, T, H, dk, dv,
                                   _p(cu_seqlens), n, h, _p(gam), _p(aqk), _p(akk), _p(tinv),
                                   _p(w), _p(u), _stream(stream))
+
+
+def kda_debug_umma(A, B, D, M, N, K, a_mode=0, b_mode=0, pack=0, dev_status=None,
+                   stream=None) -> int:
+    return load().kda_debug_umma(_p(A), _p(B), _p(D), M, N, K, a_mode, b_mode, pack,
+                                 _p(dev_status), _stream(stream))
 
 
 def forward(q, k, v, g_logit, beta, init_state=None, cu_seqlens=None, scale=1.0,

@@ -168,6 +168,21 @@ kda_status kda_debug_intra(const uint16_t* q, const uint16_t* k, const uint16_t*
                            float* gam, float* aqk, float* akk, float* tinv, float* w,
                            float* u, kda_stream_t stream);
 
+/*
+ * Test hook: one tcgen05 tile product D = A * B^T (bf16 in, fp32 out) with
+ * the operand layouts the tensor-core path uses, to check descriptors and
+ * lane placement.  A [M][K], B [N][K] row-major bf16 device buffers; D
+ * [128][N] fp32 receives all 128 accumulator lanes (lanes an M = 64 tile
+ * does not write hold a NaN marker).  M in {64, 128}; N in 16..256 and K in
+ * 16..128, multiples of 16.  a_mode: 0 shared K-major, 1 shared MN-major,
+ * 2 tensor memory (M = 128 only); b_mode: 0 K-major, 1 MN-major; pack:
+ * order of the 8x16-byte core matrices (0: along K first, 1: along M/N
+ * first).  One CTA; asynchronous on `stream`.
+ */
+kda_status kda_debug_umma(const uint16_t* A, const uint16_t* B, float* D, int M, int N, int K,
+                          int a_mode, int b_mode, int pack, int32_t* dev_status,
+                          kda_stream_t stream);
+
 /* The path kda_chunk_fwd_ex would take for these arguments: KDA_ALGO_SIMT
  * or KDA_ALGO_TC, or -1 if the combination is unsupported. */
 int kda_resolve_algo(int dtype, int dk, int dv, int chunk_size, int algo);
