@@ -1,11 +1,758 @@
-// kda_tc.cu -- tensor-core (tcgen05/TMEM/TMA) fused KDA forward.
-#include "kda_common.cuh"
+// kda_tc.cu -- fused KDA chunked forward on the Blackwell tensor cores
+// (tcgen05 + tensor memory + TMA), bf16 inputs, dk = dv = 128, 64-token
+// chunks, fp32 state and accumulation.
+//
+// One CTA owns one (sequence, head, half of the value channels) and walks
+// its sequence chunk by chunk; the two halves of a head run as independent
+// CTAs (the intra-chunk work is repeated, the state work is split).  The
+// state half S (128 key channels x 64 value channels, fp32) lives in tensor
+// memory for the whole sequence.
+//
+// Per chunk (C = 64 rows r, key channel j, 16-token tiles a = r / 16):
+//   alpha_r = max(1 / (1 + e^{x_r}), e^-5)   [= exp(max(-softplus(x), -5))]
+//   E_r = prod of alpha from the start of r's tile to r      (in [e^-80, 1])
+//   F_r = prod of alpha after r to the end of r's tile
+//   P_a = product over tile a;   gamma_r = e^{G_r} = E_r prod_{c<a} P_c
+// Gram matrices, column tile b (reference: cumulative decay at the end of
+// tile b), rows r in tiles a >= b:
+//   A_qk[r, i] = (q_r E_r m_ab) . (k_i F_i),  A_kk likewise with k_r, beta_r
+//   m_aa = 1 / P_a (<= e^80),  m_ab = prod_{b<c<a} P_c for a > b (<= 1)
+// so every factor stays inside the bf16/fp32 range: the 16-token bound on
+// the cumulative log-decay (Kimi K3 architecture, orkas.ai, "A lower bound
+// that erased a GPU code path") is what keeps m_aa below e^80, and lets the
+// diagonal tiles go through the same dense product as the others.
+// Then  T = (I + A_kk)^{-1}  (CUDA cores, fp32, blocked by 16x16 tiles),
+//   W = T (beta K gamma),  U = T (beta V),  Delta = U - W S,
+//   O = (Q gamma) S + A_qk Delta,  S <- gamma_C S + (K e^{G_C - G})^T Delta.
+// The inter-chunk recurrence is serial over chunks (Towards AI walkthrough,
+// "Infrastructure co-design": the chunk-to-chunk state dependency); the
+// state stays on chip between chunks.
+//
+// Tensor-core products per chunk (M = 128 everywhere, bf16 operands in
+// shared memory, fp32 accumulators in tensor memory):
+//   Grams   4 x [128 x 16 x 128]   A_b (rows of tiles >= b) . Ktil_b^T
+//   W^T     [128 x 64 x 64]        (beta K gamma)^T . T^T
+//   U       [128 x 64 x 64]        [T; -] . (beta V)  (rows 64.. unused)
+//   P       [128 x 64 x 128]       [W; Q gamma] . S   -> [W S; Q gamma S]
+//   S      += [128 x 64 x 64]      (K dec)^T . Delta
+//   O      += [128 x 64 x 64]      [-; A_qk] . Delta   (into P's lower rows)
+#include <cudaTypedefs.h>
+#include <stdio.h>
 
-bool kda_tc_supported(int dk, int dv) { (void)dk; (void)dv; return false; }
+#include "kda_common.cuh"
+#include "sm100.cuh"
+
+namespace {
+
+constexpr int DK = 128, DV = 128, DVH = 64, C = 64;
+constexpr int kThreads = 256;
+
+// ---- shared memory map (bytes) ---------------------------------------------
+// R0: TMA landing zone for one chunk (128B-swizzled rows of 64 channels)
+constexpr int OFF_Q = 0;          // 2 x [64 rows][128 B]
+constexpr int OFF_K = 16384;
+constexpr int OFF_G = 32768;
+constexpr int OFF_V = 49152;      // [64 rows][128 B] (this CTA's 64 value channels)
+constexpr int R0_BYTES = 57344;
+// R1: Gram operands, then (after the Gram products) the per-chunk scratch
+constexpr int OFF_R1 = R0_BYTES;
+constexpr int OFF_AB0 = OFF_R1;               // A_0: 128 M-rows -> 32768
+constexpr int OFF_AB1 = OFF_AB0 + 32768;      // A_1:  96 M-rows -> 24576
+constexpr int OFF_AB2 = OFF_AB1 + 24576;      // A_2:  64 M-rows -> 16384
+constexpr int OFF_AB3 = OFF_AB2 + 16384;      // A_3:  32 M-rows ->  8192
+constexpr int OFF_KT = OFF_AB3 + 8192;        // Ktil: 4 blocks x 4096
+constexpr int R1_BYTES = 98304;
+//   overlay after the Gram products:
+constexpr int AKK_LD = 68;                        // fp32 row stride (floats)
+constexpr int OFF_AKK = OFF_R1;                   // [64][68] fp32   17408
+constexpr int OFF_TF = OFF_AKK + 17408;           // [64][68] fp32   17408
+constexpr int OFF_Y = OFF_TF + 17408;             // [3][16][17] fp32 3264 -> 4096
+constexpr int OFF_T = OFF_Y + 4096;               // T bf16 K-major   8192
+constexpr int OFF_SB = OFF_T + 8192;              // S bf16 MN-major 16384
+constexpr int OFF_DL = OFF_SB + 16384;            // Delta bf16 MN    8192
+constexpr int OFF_X = OFF_DL + 8192;              // rows 0..63 of [-; A_qk]
+constexpr int OFF_AQ = OFF_X + 8192;              // A_qk masked bf16 8192
+constexpr int OFF_BV = OFF_AQ + 8192;             // (beta V)^T bf16  8192
+static_assert(OFF_BV + 8192 <= OFF_R1 + R1_BYTES, "R1 overlay");
+// R2: [W; Q gamma] MN-major, 128 M-rows x 128 K
+constexpr int OFF_WQ = OFF_R1 + R1_BYTES;
+// R3: (beta K gamma)^T and (K dec)^T, K-major 128 x 64
+constexpr int OFF_BKG = OFF_WQ + 32768;
+constexpr int OFF_KD = OFF_BKG + 16384;
+// small
+constexpr int OFF_BETA = OFF_KD + 16384;          // 64 fp32
+constexpr int OFF_PT = OFF_BETA + 256;            // [4][128] fp32 tile products
+constexpr int OFF_GC = OFF_PT + 2048;             // [128] fp32 gamma_C
+constexpr int OFF_BAR = OFF_GC + 512;             // mbarriers
+constexpr int OFF_MISC = OFF_BAR + 64;            // tmem base, abort flag
+constexpr int SMEM_BYTES = OFF_MISC + 64;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+// TMEM columns
+constexpr uint32_t TM_S = 0, TM_P = 64, TM_U = 128, TM_W = 192, TM_G = 256;
+constexpr uint32_t TM_COLS = 512;
+
+constexpr uint32_t TX_BYTES = 57344;  // Q, K, G (2 boxes each) + V (1 box)
+
+// ---- operand layouts (core matrices of 8 x 16 B) ---------------------------
+// MN-major: element (mn, k) with `lbo` the K-group stride, M/N groups 128 B apart
+__device__ __forceinline__ uint32_t mn_off(int mn, int k, uint32_t lbo) {
+  return (uint32_t)(mn >> 3) * 128u + (uint32_t)(k >> 3) * lbo + (uint32_t)(k & 7) * 16u +
+         (uint32_t)(mn & 7) * 2u;
+}
+// K-major with K extent 64: K groups 128 B apart, M/N groups 1024 B apart
+__device__ __forceinline__ uint32_t k64_off(int mn, int k) {
+  return (uint32_t)(mn >> 3) * 1024u + (uint32_t)(k >> 3) * 128u + (uint32_t)(mn & 7) * 16u +
+         (uint32_t)(k & 7) * 2u;
+}
+// 128B-swizzled TMA row: element (row, ch) of a [rows][64] bf16 box
+__device__ __forceinline__ uint32_t sw128_off(int row, int ch) {
+  return (uint32_t)row * 128u + (uint32_t)(((ch >> 3) ^ (row & 7)) << 4) + (uint32_t)(ch & 7) * 2u;
+}
+__device__ __forceinline__ float ld_bf16(const unsigned char* base, uint32_t off) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + off));
+}
+
+__device__ __forceinline__ void st16(unsigned char* p, uint32_t a, uint32_t b, uint32_t c,
+                                     uint32_t d) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
+// pack 8 floats (v[0..7]) into a 16-byte chunk of bf16
+__device__ __forceinline__ void st8_bf16(unsigned char* p, const float* v) {
+  st16(p, sm100::pack_bf16x2(v[0], v[1]), sm100::pack_bf16x2(v[2], v[3]),
+       sm100::pack_bf16x2(v[4], v[5]), sm100::pack_bf16x2(v[6], v[7]));
+}
+
+struct TcParams {
+  kda::FwdParams p;
+  // debug dump of one (n, h): per chunk [64][.] fp32
+  int dbg_n, dbg_h;
+  float *dbg_gam, *dbg_aqk, *dbg_akk, *dbg_t, *dbg_w, *dbg_u;
+};
+
+__device__ __forceinline__ float alpha_of(float x) {
+  // exp(max(-softplus(x), -5)) = max(sigmoid(-x), e^-5)
+  const float e = __expf(x);
+  return fmaxf(__fdividef(1.0f, 1.0f + e), 0.006737946999085467f);
+}
+
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    kda_tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_g,
+                        const __grid_constant__ CUtensorMap tm_v, const TcParams tp) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const kda::FwdParams& p = tp.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int half = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+  const int H = p.H;
+
+  uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* bar_mma = bar_tma + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  int* s_abort = reinterpret_cast<int*>(smem + OFF_MISC + 4);
+  float* s_beta = reinterpret_cast<float*>(smem + OFF_BETA);
+  float* s_pt = reinterpret_cast<float*>(smem + OFF_PT);
+  float* s_gc = reinterpret_cast<float*>(smem + OFF_GC);
+  float* s_akk = reinterpret_cast<float*>(smem + OFF_AKK);
+  float* s_tf = reinterpret_cast<float*>(smem + OFF_TF);
+  float* s_y = reinterpret_cast<float*>(smem + OFF_Y);
+
+  int64_t row_base, t0, t1;
+  if (!kda::seq_span(p, n, row_base, t0, t1)) return;  // uniform over the CTA
+
+  if (warp == 0) {
+    sm100::tmem_alloc(s_tmem, TM_COLS);
+    sm100::tmem_relinquish();
+  }
+  if (tid == 32) {
+    sm100::mbar_init(bar_tma, 1);
+    sm100::mbar_init(bar_mma, 1);
+    sm100::fence_mbar_init();
+    if (t1 > t0) {
+      sm100::tma_prefetch_desc(&tm_q);
+      sm100::tma_prefetch_desc(&tm_k);
+      sm100::tma_prefetch_desc(&tm_g);
+      sm100::tma_prefetch_desc(&tm_v);
+    }
+  }
+  if (tid == 0) *s_abort = 0;
+  sm100::tc_fence_before();
+  __syncthreads();
+  sm100::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t lane_q = 32u * (warp & 3);  // this warp's TMEM lane quarter
+  const int64_t sbase = ((int64_t)n * H + h) * (int64_t)DK * DV + half * DVH;
+
+  // ---- initial state half into TMEM (lane = key channel) -------------------
+  if (warp < 4) {
+    const int i = warp * 32 + lane;
+    for (int c = 0; c < DVH; c += 16) {
+      uint32_t r[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        r[e] = __float_as_uint(p.init_state ? p.init_state[sbase + (int64_t)i * DV + c + e]
+                                            : 0.0f);
+      sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + c), r);
+    }
+    sm100::tmem_wait_st();
+  }
+
+  const int64_t nchunks = (t1 - t0 + C - 1) / C;
+  uint32_t mma_phase = 0;
+  bool mma_inflight = false;
+  auto issue_tma = [&](int64_t ci) {
+    const int row = (int)(row_base + t0 + ci * C);
+    sm100::mbar_arrive_expect_tx(bar_tma, TX_BYTES);
+    sm100::tma_load_3d(smem + OFF_Q, &tm_q, bar_tma, 0, h, row);
+    sm100::tma_load_3d(smem + OFF_Q + 8192, &tm_q, bar_tma, 64, h, row);
+    sm100::tma_load_3d(smem + OFF_K, &tm_k, bar_tma, 0, h, row);
+    sm100::tma_load_3d(smem + OFF_K + 8192, &tm_k, bar_tma, 64, h, row);
+    sm100::tma_load_3d(smem + OFF_G, &tm_g, bar_tma, 0, h, row);
+    sm100::tma_load_3d(smem + OFF_G + 8192, &tm_g, bar_tma, 64, h, row);
+    sm100::tma_load_3d(smem + OFF_V, &tm_v, bar_tma, half * DVH, h, row);
+  };
+  // wait for the MMA batch just committed; records a timeout
+  auto wait_mma = [&]() {
+    const bool ok = sm100::mbar_wait(bar_mma, mma_phase & 1);
+    if (ok) ++mma_phase;
+    mma_inflight = !ok;
+    if (!ok) {
+      *s_abort = 1;
+      if (p.dev_status) atomicExch(p.dev_status, (int32_t)KDA_ERR_TIMEOUT);
+    }
+    sm100::tc_fence_after();
+  };
+  auto commit_mma = [&]() { sm100::mma_commit(bar_mma); };
+  auto sync_all = [&]() {
+    sm100::tc_fence_before();
+    __syncthreads();
+    sm100::tc_fence_after();
+  };
+
+  if (tid == 0 && nchunks > 0) issue_tma(0);
+  bool tma_pending = nchunks > 0;  // a load into the landing zone is in flight
+  uint32_t tma_parity = 0;
+
+  for (int64_t ci = 0; ci < nchunks; ++ci) {
+    const int64_t cs = t0 + ci * C;
+    const int L = (t1 - cs) < C ? (int)(t1 - cs) : C;
+    const bool dbg_nh = tp.dbg_gam && n == tp.dbg_n && h == tp.dbg_h;
+    const bool dbg = dbg_nh && half == 0;
+    const int64_t dbo = ci * C;  // debug row offset
+
+    // ---- (A) inputs of this chunk ------------------------------------------
+    if (tid < C) {
+      float b = 0.0f;
+      if (tid < L) b = __bfloat162float(
+          static_cast<const __nv_bfloat16*>(p.beta)[(row_base + cs + tid) * H + h]);
+      s_beta[tid] = b;
+    }
+    {
+      const bool ok = sm100::mbar_wait(bar_tma, (uint32_t)(ci & 1));
+      if (!ok) {
+        *s_abort = 1;
+        if (p.dev_status) atomicExch(p.dev_status, (int32_t)KDA_ERR_TIMEOUT);
+      }
+      tma_pending = !ok;
+      tma_parity = (uint32_t)(ci & 1);
+    }
+    __syncthreads();
+    if (*s_abort) break;
+
+    // ---- (B) gate: one key channel j, two tiles per thread ------------------
+    {
+      const int j = tid & 127, pr = tid >> 7;  // tiles 2pr, 2pr+1
+      const unsigned char* sq = smem + OFF_Q + (j >> 6) * 8192;
+      const unsigned char* sk = smem + OFF_K + (j >> 6) * 8192;
+      const unsigned char* sg = smem + OFF_G + (j >> 6) * 8192;
+      const int jc = j & 63;
+      float al[2][16];
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const int a = 2 * pr + tt;
+        float prod = 1.0f;
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+          const int r = 16 * a + s;
+          const float x = ld_bf16(sg, sw128_off(r, jc));
+          const float av = (r < L) ? alpha_of(x) : 1.0f;
+          al[tt][s] = av;
+          prod *= av;
+        }
+        s_pt[a * 128 + j] = prod;
+      }
+      __syncthreads();
+      const float P0 = s_pt[j], P1 = s_pt[128 + j], P2 = s_pt[256 + j], P3 = s_pt[384 + j];
+      const float Pv[4] = {P0, P1, P2, P3};
+      if (pr == 0) s_gc[j] = P0 * P1 * P2 * P3;
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const int a = 2 * pr + tt;
+        float pre = 1.0f, post = 1.0f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (c < a) pre *= Pv[c];
+          if (c > a) post *= Pv[c];
+        }
+        float m[4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          float mm = 1.0f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (c > b && c < a) mm *= Pv[c];
+          m[b] = (b == a) ? __fdividef(1.0f, Pv[a]) : mm;
+        }
+        float E[16], F[16];
+        {
+          float e = 1.0f;
+#pragma unroll
+          for (int s = 0; s < 16; ++s) { e *= al[tt][s]; E[s] = e; }
+          float f = 1.0f;
+#pragma unroll
+          for (int s = 15; s >= 0; --s) { F[s] = f; f *= al[tt][s]; }
+        }
+#pragma unroll
+        for (int hg = 0; hg < 2; ++hg) {  // rows 8hg .. 8hg+7 of the tile
+          float qv[8], kv[8], bv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int r = 16 * a + 8 * hg + e;
+            const bool ok = r < L;
+            qv[e] = ok ? ld_bf16(sq, sw128_off(r, jc)) * p.scale : 0.0f;
+            kv[e] = ok ? ld_bf16(sk, sw128_off(r, jc)) : 0.0f;
+            bv[e] = s_beta[r];
+          }
+          float t[8];
+          // Gram row operands for every column tile b <= a
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            if (b > a) continue;
+            const int Rb = 128 - 32 * b;
+            unsigned char* base = smem + OFF_AB0 + (b == 0 ? 0 : b == 1 ? 32768
+                                                               : b == 2 ? 57344 : 73728);
+            const uint32_t lbo = (uint32_t)Rb * 16u;
+            const int mq = 32 * (a - b) + 8 * hg;       // local M-row of q rows
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t[e] = qv[e] * E[8 * hg + e] * m[b];
+            st8_bf16(base + mn_off(mq, j, lbo), t);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t[e] = kv[e] * E[8 * hg + e] * m[b];
+            st8_bf16(base + mn_off(mq + 16, j, lbo), t);
+          }
+          // Ktil (B of the Gram product of column tile a): k F
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t[e] = kv[e] * F[8 * hg + e];
+          st8_bf16(smem + OFF_KT + a * 4096 + mn_off(8 * hg, j, 256), t);
+          // Q gamma into rows 64.. of [W; Q gamma]
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t[e] = qv[e] * E[8 * hg + e] * pre;
+          st8_bf16(smem + OFF_WQ + mn_off(64 + 16 * a + 8 * hg, j, 2048), t);
+          // (beta K gamma)^T, K-major [j][r]
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t[e] = bv[e] * kv[e] * E[8 * hg + e] * pre;
+          st8_bf16(smem + OFF_BKG + k64_off(j, 16 * a + 8 * hg), t);
+          // (K e^{G_C - G})^T, K-major [j][r]
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t[e] = kv[e] * F[8 * hg + e] * post;
+          st8_bf16(smem + OFF_KD + k64_off(j, 16 * a + 8 * hg), t);
+          if (dbg && tp.dbg_gam) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int r = 16 * a + 8 * hg + e;
+              tp.dbg_gam[(dbo + r) * DK + j] = E[8 * hg + e] * pre;
+            }
+          }
+        }
+      }
+    }
+    sm100::fence_async_smem();
+    sync_all();
+
+    // ---- (C) Gram products --------------------------------------------------
+    if (tid == 0) {
+      const uint32_t idesc = sm100::idesc_bf16(128, 16, 1, 1);
+      const uint32_t abase[4] = {0u, 32768u, 57344u, 73728u};
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t lbo = (uint32_t)(128 - 32 * b) * 16u;
+        const uint32_t sa = sm100::smem_u32(smem + OFF_AB0 + abase[b]);
+        const uint32_t sb = sm100::smem_u32(smem + OFF_KT + b * 4096);
+#pragma unroll
+        for (int s = 0; s < DK / 16; ++s) {
+          const uint64_t ad = sm100::smem_desc(sa + s * 2 * lbo, lbo, 128);
+          const uint64_t bd = sm100::smem_desc(sb + s * 2 * 256, 256, 128);
+          sm100::mma_ss(tmem + TM_G + 16 * b, ad, bd, idesc, s > 0);
+        }
+      }
+      commit_mma();
+    }
+    wait_mma();
+
+    // ---- (D) Gram epilogue (warps 0-3) | S half and (beta V)^T (warps 4-7) --
+    if (warp < 4) {
+      const int l = tid;  // TMEM lane
+#pragma unroll 1
+      for (int b = 0; b < 4; ++b) {
+        float v[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_G + 16 * b), v);
+        sm100::tmem_wait_ld();
+        const int m = l + 32 * b;
+        if (m < 128) {
+          const int a = m >> 5, s = m & 31, r = 16 * a + (s & 15);
+          if (s < 16) {  // A_qk row r, columns of tile b, inclusive mask
+            float t[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) t[c] = (16 * b + c <= r) ? v[c] : 0.0f;
+            unsigned char* base = smem + OFF_AQ;
+            st8_bf16(base + k64_off(r, 16 * b), t);
+            st8_bf16(base + k64_off(r, 16 * b + 8), t + 8);
+            if (b == a) {
+              const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+              for (int bb = a + 1; bb < 4; ++bb) {
+                st8_bf16(base + k64_off(r, 16 * bb), z);
+                st8_bf16(base + k64_off(r, 16 * bb + 8), z);
+              }
+            }
+            if (dbg && tp.dbg_aqk) {
+              for (int c = 0; c < 16; ++c) tp.dbg_aqk[(dbo + r) * C + 16 * b + c] = t[c];
+              if (b == a)
+                for (int c = 16 * (a + 1); c < C; ++c) tp.dbg_aqk[(dbo + r) * C + c] = 0.0f;
+            }
+          } else {       // beta_r A_kk row r, strict mask, fp32 for the solve
+            const float br = s_beta[r];
+            float* row = s_akk + r * AKK_LD + 16 * b;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) row[c] = (16 * b + c < r) ? br * v[c] : 0.0f;
+          }
+        }
+      }
+    } else {
+      const int i = tid - 128;  // key channel = TMEM lane
+      float sv[64];
+#pragma unroll
+      for (int c = 0; c < 64; c += 16) {
+        float v[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c), v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sv[c + e] = v[e];
+      }
+      sm100::tmem_wait_ld();
+      // bf16 copy of S (B of the P product, MN-major: K = key channel i)
+#pragma unroll
+      for (int jg = 0; jg < 8; ++jg) st8_bf16(smem + OFF_SB + mn_off(8 * jg, i, 1024), sv + 8 * jg);
+      // S <- gamma_C * S ahead of the rank-64 update
+      const float gc = s_gc[i];
+#pragma unroll
+      for (int c = 0; c < 64; c += 16) {
+        uint32_t r[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(gc * sv[c + e]);
+        sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + c), r);
+      }
+      sm100::tmem_wait_st();
+      // (beta V)^T, K-major [value channel jv][row r]
+      const int jv = i & 63, rh = i >> 6;  // rows 32rh .. 32rh+31
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
+        float t[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int r = 32 * rh + 8 * g8 + e;
+          t[e] = (r < L) ? s_beta[r] * ld_bf16(smem + OFF_V, sw128_off(r, jv)) : 0.0f;
+        }
+        st8_bf16(smem + OFF_BV + k64_off(jv, 32 * rh + 8 * g8), t);
+      }
+    }
+    sm100::fence_async_smem();
+    sync_all();
+    // the landing zone is free: prefetch the next chunk
+    if (ci + 1 < nchunks) {
+      if (tid == 0) issue_tma(ci + 1);
+      tma_pending = true;
+      tma_parity = (uint32_t)((ci + 1) & 1);
+    }
+
+    // ---- (E) T = (I + A_kk)^{-1}, fp32, blocked by 16 x 16 tiles -----------
+    if (tid < 64) {  // diagonal tiles: thread = (tile, column)
+      const int blk = tid >> 4, c = tid & 15;
+      const float* A = s_akk + (16 * blk) * AKK_LD + 16 * blk;
+      float x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float acc = (r == c) ? 1.0f : 0.0f;
+        if (r > c) {
+#pragma unroll
+          for (int k2 = 0; k2 < 16; ++k2)
+            if (k2 >= c && k2 < r) acc = fmaf(-A[r * AKK_LD + k2], x[k2], acc);
+        }
+        x[r] = acc;
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) s_tf[(16 * blk + r) * AKK_LD + 16 * blk + c] = x[r];
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int d = 1; d < 4; ++d) {
+      const int nblk = 4 - d;  // tiles (b + d, b), b = 0 .. nblk-1
+      // Y = A[a, b .. a-1] . T[b .. a-1, b]
+      for (int e = tid; e < nblk * 256; e += kThreads) {
+        const int b = e >> 8, r = (e >> 4) & 15, c = e & 15, a = b + d;
+        const float* Ar = s_akk + (16 * a + r) * AKK_LD;
+        float acc = 0.0f;
+        for (int k2 = 16 * b; k2 < 16 * a; ++k2)
+          acc = fmaf(Ar[k2], s_tf[k2 * AKK_LD + 16 * b + c], acc);
+        s_y[(b * 16 + r) * 17 + c] = acc;
+      }
+      __syncthreads();
+      // T[a, b] = -T[a, a] . Y
+      for (int e = tid; e < nblk * 256; e += kThreads) {
+        const int b = e >> 8, r = (e >> 4) & 15, c = e & 15, a = b + d;
+        const float* Tr = s_tf + (16 * a + r) * AKK_LD + 16 * a;
+        float acc = 0.0f;
+        for (int k2 = 0; k2 <= r; ++k2) acc = fmaf(Tr[k2], s_y[(b * 16 + k2) * 17 + c], acc);
+        s_tf[(16 * a + r) * AKK_LD + 16 * b + c] = -acc;
+      }
+      __syncthreads();
+    }
+    // T as bf16, K-major [r][i], unit diagonal, zero above
+    for (int e = tid; e < 512; e += kThreads) {
+      const int r = e >> 3, i0 = (e & 7) * 8;
+      float t[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int i = i0 + c;
+        t[c] = (i < r) ? s_tf[r * AKK_LD + i] : (i == r ? 1.0f : 0.0f);
+      }
+      st8_bf16(smem + OFF_T + k64_off(r, i0), t);
+      if (dbg && tp.dbg_t)
+        for (int c = 0; c < 8; ++c) tp.dbg_t[(dbo + r) * C + i0 + c] = t[c];
+      if (dbg && tp.dbg_akk)
+        for (int c = 0; c < 8; ++c) tp.dbg_akk[(dbo + r) * C + i0 + c] = s_akk[r * AKK_LD + i0 + c];
+    }
+    sm100::fence_async_smem();
+    sync_all();
+
+    // ---- (F) W^T and U products --------------------------------------------
+    if (tid == 0) {
+      const uint32_t idesc = sm100::idesc_bf16(128, 64, 0, 0);
+      const uint32_t s_bkg = sm100::smem_u32(smem + OFF_BKG);
+      const uint32_t s_t = sm100::smem_u32(smem + OFF_T);
+      const uint32_t s_bv = sm100::smem_u32(smem + OFF_BV);
+#pragma unroll
+      for (int s = 0; s < C / 16; ++s) {
+        sm100::mma_ss(tmem + TM_W, sm100::smem_desc(s_bkg + 256 * s, 128, 1024),
+                      sm100::smem_desc(s_t + 256 * s, 128, 1024), idesc, s > 0);
+      }
+#pragma unroll
+      for (int s = 0; s < C / 16; ++s) {
+        sm100::mma_ss(tmem + TM_U, sm100::smem_desc(s_t + 256 * s, 128, 1024),
+                      sm100::smem_desc(s_bv + 256 * s, 128, 1024), idesc, s > 0);
+      }
+      commit_mma();
+    }
+    wait_mma();
+
+    // ---- (G) W rows into [W; Q gamma] (warps 0-3, lane = key channel) -------
+    if (warp < 4) {
+      const int j = tid;
+      float wv[64];
+#pragma unroll
+      for (int c = 0; c < 64; c += 16) {
+        float v[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_W + c), v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) wv[c + e] = v[e];
+      }
+      sm100::tmem_wait_ld();
+#pragma unroll
+      for (int rg = 0; rg < 8; ++rg) st8_bf16(smem + OFF_WQ + mn_off(8 * rg, j, 2048), wv + 8 * rg);
+      if (dbg && tp.dbg_w)
+        for (int r = 0; r < C; ++r) tp.dbg_w[(dbo + r) * DK + j] = wv[r];
+    } else if (dbg_nh && tp.dbg_u && warp < 6) {
+      const int r = tid - 128;  // lanes 0..63 of U
+      for (int c = 0; c < 64; c += 16) {
+        float v[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_U + c), v);
+        sm100::tmem_wait_ld();
+        for (int e = 0; e < 16; ++e) tp.dbg_u[(dbo + r) * DV + half * DVH + c + e] = v[e];
+      }
+    }
+    sm100::fence_async_smem();
+    sync_all();
+
+    // ---- (H) P = [W; Q gamma] . S -------------------------------------------
+    if (tid == 0) {
+      const uint32_t idesc = sm100::idesc_bf16(128, 64, 1, 1);
+      const uint32_t sa = sm100::smem_u32(smem + OFF_WQ);
+      const uint32_t sb = sm100::smem_u32(smem + OFF_SB);
+#pragma unroll
+      for (int s = 0; s < DK / 16; ++s)
+        sm100::mma_ss(tmem + TM_P, sm100::smem_desc(sa + s * 4096, 2048, 128),
+                      sm100::smem_desc(sb + s * 2048, 1024, 128), idesc, s > 0);
+      commit_mma();
+    }
+    wait_mma();
+
+    // ---- (I) Delta = U - W S (warps 0-1, lane = row) ------------------------
+    if (warp < 2) {
+      const int r = tid;
+      float dv[64];
+#pragma unroll
+      for (int c = 0; c < 64; c += 16) {
+        float ws[16], u[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_P + c), ws);
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_U + c), u);
+        sm100::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dv[c + e] = u[e] - ws[e];
+      }
+#pragma unroll
+      for (int jg = 0; jg < 8; ++jg) st8_bf16(smem + OFF_DL + mn_off(8 * jg, r, 1024), dv + 8 * jg);
+    }
+    sm100::fence_async_smem();
+    sync_all();
+
+    // ---- (J) S += (K dec)^T Delta;  O += A_qk Delta ---------------------------
+    if (tid == 0) {
+      const uint32_t id_s = sm100::idesc_bf16(128, 64, 0, 1);
+      const uint32_t s_kd = sm100::smem_u32(smem + OFF_KD);
+      const uint32_t s_x = sm100::smem_u32(smem + OFF_X);
+      const uint32_t s_dl = sm100::smem_u32(smem + OFF_DL);
+#pragma unroll
+      for (int s = 0; s < C / 16; ++s)
+        sm100::mma_ss(tmem + TM_S, sm100::smem_desc(s_kd + 256 * s, 128, 1024),
+                      sm100::smem_desc(s_dl + s * 2048, 1024, 128), id_s, 1);
+#pragma unroll
+      for (int s = 0; s < C / 16; ++s)
+        sm100::mma_ss(tmem + TM_P, sm100::smem_desc(s_x + 256 * s, 128, 1024),
+                      sm100::smem_desc(s_dl + s * 2048, 1024, 128), id_s, 1);
+      commit_mma();
+    }
+    wait_mma();
+
+    // ---- (K) output rows (warps 2-3, lanes 64..127 = row r) ------------------
+    if (warp == 2 || warp == 3) {
+      const int r = tid - 64;
+      float o[64];
+#pragma unroll
+      for (int c = 0; c < 64; c += 16) {
+        float v[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_P + c), v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[c + e] = v[e];
+      }
+      sm100::tmem_wait_ld();
+      if (r < L) {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
+                             ((row_base + cs + r) * H + h) * DV + half * DVH;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          uint4 w = make_uint4(sm100::pack_bf16x2(o[8 * g], o[8 * g + 1]),
+                               sm100::pack_bf16x2(o[8 * g + 2], o[8 * g + 3]),
+                               sm100::pack_bf16x2(o[8 * g + 4], o[8 * g + 5]),
+                               sm100::pack_bf16x2(o[8 * g + 6], o[8 * g + 7]));
+          *reinterpret_cast<uint4*>(dst + 8 * g) = w;
+        }
+      }
+    }
+    sync_all();
+    if (*s_abort) break;
+  }
+
+  // ---- drain anything still in flight after an abort, write the state ----
+  // bounded waits for copies and products still in flight before the TMEM
+  // is released (only after an abort; otherwise nothing is pending)
+  if (*s_abort) {
+    if (tma_pending) sm100::mbar_wait(bar_tma, tma_parity, 200000000ull);
+    if (mma_inflight) sm100::mbar_wait(bar_mma, mma_phase & 1, 200000000ull);
+  }
+  if (!*s_abort && p.final_state && warp < 4) {
+    const int i = tid;
+    for (int c = 0; c < DVH; c += 16) {
+      float v[16];
+      sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c), v);
+      sm100::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) p.final_state[sbase + (int64_t)i * DV + c + e] = v[e];
+    }
+  }
+  sm100::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) sm100::tmem_dealloc(tmem, TM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 3-D map over a [rows, H, d] bf16 tensor: box = 64 channels x 1 head x 64 rows
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H, int d) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+kda_status launch_tc(const TcParams& tp, cudaStream_t stream) {
+  const kda::FwdParams& p = tp.p;
+  const int64_t rows = p.cu_seqlens ? (int64_t)p.T : (int64_t)p.N * p.T;
+  if (rows == 0 || p.N > 65535 || p.H > 65535) {
+    if (rows != 0) return KDA_ERR_UNSUPPORTED;
+  }
+  if (rows >= (int64_t)1 << 31) return KDA_ERR_UNSUPPORTED;
+  CUtensorMap mq, mk, mg, mv;
+  // an empty batch still has states to pass through; give the maps one row
+  const int64_t mrows = rows > 0 ? rows : 1;
+  if (rows > 0) {
+    if (!make_map(&mq, p.q, mrows, p.H, DK) || !make_map(&mk, p.k, mrows, p.H, DK) ||
+        !make_map(&mg, p.g, mrows, p.H, DK) || !make_map(&mv, p.v, mrows, p.H, DV))
+      return KDA_ERR_CUDA;
+  } else {
+    memset(&mq, 0, sizeof(mq));
+    mk = mq; mg = mq; mv = mq;
+  }
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kda_tc_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    attr_set = true;
+  }
+  dim3 grid(2, p.H, p.N);
+  kda_tc_fused_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mg, mv, tp);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+bool kda_tc_supported(int dk, int dv) { return dk == DK && dv == DV; }
 
 kda_status kda_launch_tc(const kda::FwdParams& p, cudaStream_t stream) {
-  (void)p; (void)stream;
-  return KDA_ERR_UNSUPPORTED;
+  TcParams tp;
+  tp.p = p;
+  tp.dbg_n = -1;
+  tp.dbg_h = -1;
+  tp.dbg_gam = tp.dbg_aqk = tp.dbg_akk = tp.dbg_t = tp.dbg_w = tp.dbg_u = nullptr;
+  return launch_tc(tp, stream);
 }
 
 extern "C" kda_status kda_debug_intra(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -13,8 +760,33 @@ extern "C" kda_status kda_debug_intra(const uint16_t* q, const uint16_t* k, cons
                                       int T, int H, int dk, int dv, const int32_t* cu_seqlens,
                                       int n, int h, float* gam, float* aqk, float* akk,
                                       float* tinv, float* w, float* u, kda_stream_t stream) {
-  (void)q; (void)k; (void)v; (void)g_logit; (void)beta; (void)B; (void)T; (void)H; (void)dk;
-  (void)dv; (void)cu_seqlens; (void)n; (void)h; (void)gam; (void)aqk; (void)akk; (void)tinv;
-  (void)w; (void)u; (void)stream;
-  return KDA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !g_logit || !beta) return KDA_ERR_INVALID_ARG;
+  if (dk != DK || dv != DV) return KDA_ERR_UNSUPPORTED;
+  if (B < 1 || T < 1 || H < 1 || n < 0 || n >= B || h < 0 || h >= H) return KDA_ERR_INVALID_ARG;
+  // scratch outputs for the full forward
+  const int64_t rows = cu_seqlens ? (int64_t)T : (int64_t)B * T;
+  void* out = nullptr;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMallocAsync(&out, (size_t)rows * H * DV * 2, s) != cudaSuccess) return KDA_ERR_CUDA;
+  TcParams tp;
+  tp.p.q = q; tp.p.k = k; tp.p.v = v; tp.p.g = g_logit; tp.p.beta = beta;
+  tp.p.init_state = nullptr; tp.p.out = out; tp.p.final_state = nullptr;
+  tp.p.cu_seqlens = cu_seqlens; tp.p.dev_status = nullptr;
+  tp.p.N = B; tp.p.T = T; tp.p.H = H; tp.p.dk = dk; tp.p.dv = dv; tp.p.scale = 1.0f;
+  tp.dbg_n = n; tp.dbg_h = h;
+  // gam is the trigger for the dump; give it a scratch when not wanted
+  float* g_scratch = nullptr;
+  if (!gam) {
+    const int64_t len = cu_seqlens ? (int64_t)T : (int64_t)T;
+    if (cudaMallocAsync((void**)&g_scratch, (size_t)(len + C) * DK * 4, s) != cudaSuccess) {
+      cudaFreeAsync(out, s);
+      return KDA_ERR_CUDA;
+    }
+  }
+  tp.dbg_gam = gam ? gam : g_scratch;
+  tp.dbg_aqk = aqk; tp.dbg_akk = akk; tp.dbg_t = tinv; tp.dbg_w = w; tp.dbg_u = u;
+  kda_status st = launch_tc(tp, s);
+  if (g_scratch) cudaFreeAsync(g_scratch, s);
+  cudaFreeAsync(out, s);
+  return st;
 }

@@ -50,13 +50,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: returns false if the phase did not complete within
-// `max_iter` polls (each try_wait itself suspends for a while).
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: returns false if the phase has not completed after
+// `limit_ns` nanoseconds of polling (default 2 s, far above any legitimate
+// wait of these kernels).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          uint32_t max_iter = (1u << 24)) {
-  for (uint32_t i = 0; i < max_iter; ++i)
+                                          uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-  return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
 }
 
 // ---------------------------------------------------------------------------

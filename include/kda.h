@@ -155,7 +155,7 @@ size_t kda_host_staging_bytes(int B, int T, int H, int dk, int dv, int dtype, in
  * Test hooks (not part of the hot path): the intra-chunk steps of the
  * tensor-core path for one (sequence n, head h), every chunk, written to
  * fp32 device buffers laid out [n_chunks, 64, .]:
- *   gam  [., 64, dk]  cumulative log-decay from the chunk start
+ *   gam  [., 64, dk]  cumulative decay factor e^{G} from the chunk start
  *   aqk  [., 64, 64]  A_qk incl. diagonal (upper part zero)
  *   akk  [., 64, 64]  beta-weighted A_kk, strictly lower
  *   tinv [., 64, 64]  (I + A_kk)^{-1}
