@@ -94,6 +94,21 @@ constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t TX_BYTES = 57344;  // Q, K, G (2 boxes each) + V (1 box)
 
+#ifdef KDA_PHASE_TIMING
+// cycles spent in each phase of the chunk loop by thread 0 of CTA (0, 0, 0)
+__device__ unsigned long long kda_phase_cycles[16];
+#define KDA_PHASE(k)                                                           \
+  do {                                                                         \
+    if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {   \
+      const long long t_ = clock64();                                          \
+      kda_phase_cycles[k] += (unsigned long long)(t_ - t_phase);               \
+      t_phase = t_;                                                            \
+    }                                                                          \
+  } while (0)
+#else
+#define KDA_PHASE(k) do { } while (0)
+#endif
+
 // ---- operand layouts (core matrices of 8 x 16 B) ---------------------------
 // MN-major: element (mn, k) with `lbo` the K-group stride, M/N groups 128 B apart
 __device__ __forceinline__ uint32_t mn_off(int mn, int k, uint32_t lbo) {
@@ -235,6 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool tma_pending = nchunks > 0;  // a load into the landing zone is in flight
   uint32_t tma_parity = 0;
 
+#ifdef KDA_PHASE_TIMING
+  long long t_phase = clock64();
+#endif
   for (int64_t ci = 0; ci < nchunks; ++ci) {
     const int64_t cs = t0 + ci * C;
     const int L = (t1 - cs) < C ? (int)(t1 - cs) : C;
@@ -259,6 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_parity = (uint32_t)(ci & 1);
     }
     __syncthreads();
+    KDA_PHASE(0);
     if (*s_abort) break;
 
     // ---- (B) gate: one key channel j, two tiles per thread ------------------
@@ -370,6 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     sm100::fence_async_smem();
     sync_all();
+    KDA_PHASE(1);
 
     // ---- (C) Gram products --------------------------------------------------
     if (tid == 0) {
@@ -390,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       commit_mma();
     }
     wait_mma();
+    KDA_PHASE(2);
 
     // ---- (D) Gram epilogue (warps 0-3) | S half and (beta V)^T (warps 4-7) --
     if (warp < 4) {
@@ -468,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     sm100::fence_async_smem();
     sync_all();
+    KDA_PHASE(3);
     // the landing zone is free: prefetch the next chunk
     if (ci + 1 < nchunks) {
       if (tid == 0) issue_tma(ci + 1);
@@ -530,10 +552,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (dbg && tp.dbg_t)
         for (int c = 0; c < 8; ++c) tp.dbg_t[(dbo + r) * C + i0 + c] = t[c];
       if (dbg && tp.dbg_akk)
-        for (int c = 0; c < 8; ++c) tp.dbg_akk[(dbo + r) * C + i0 + c] = s_akk[r * AKK_LD + i0 + c];
+        for (int c = 0; c < 8; ++c)
+          tp.dbg_akk[(dbo + r) * C + i0 + c] = (i0 + c < r) ? s_akk[r * AKK_LD + i0 + c] : 0.0f;
     }
     sm100::fence_async_smem();
     sync_all();
+    KDA_PHASE(4);
 
     // ---- (F) W^T and U products --------------------------------------------
     if (tid == 0) {
@@ -554,6 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       commit_mma();
     }
     wait_mma();
+    KDA_PHASE(5);
 
     // ---- (G) W rows into [W; Q gamma] (warps 0-3, lane = key channel) -------
     if (warp < 4) {
@@ -582,6 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     sm100::fence_async_smem();
     sync_all();
+    KDA_PHASE(6);
 
     // ---- (H) P = [W; Q gamma] . S -------------------------------------------
     if (tid == 0) {
@@ -595,6 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       commit_mma();
     }
     wait_mma();
+    KDA_PHASE(7);
 
     // ---- (I) Delta = U - W S (warps 0-1, lane = row) ------------------------
     if (warp < 2) {
@@ -614,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     sm100::fence_async_smem();
     sync_all();
+    KDA_PHASE(8);
 
     // ---- (J) S += (K dec)^T Delta;  O += A_qk Delta ---------------------------
     if (tid == 0) {
@@ -632,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       commit_mma();
     }
     wait_mma();
+    KDA_PHASE(9);
 
     // ---- (K) output rows (warps 2-3, lanes 64..127 = row r) ------------------
     if (warp == 2 || warp == 3) {
@@ -659,6 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     sync_all();
+    KDA_PHASE(10);
     if (*s_abort) break;
   }
 
@@ -743,6 +773,19 @@ kda_status launch_tc(const TcParams& tp, cudaStream_t stream) {
 }
 
 }  // namespace
+
+#ifdef KDA_PHASE_TIMING
+extern "C" int kda_phase_timing_read(unsigned long long* out16, int reset) {
+  if (cudaMemcpyFromSymbol(out16, kda_phase_cycles, sizeof(unsigned long long) * 16) !=
+      cudaSuccess)
+    return -1;
+  if (reset) {
+    unsigned long long z[16] = {0};
+    cudaMemcpyToSymbol(kda_phase_cycles, z, sizeof(z));
+  }
+  return 0;
+}
+#endif
 
 bool kda_tc_supported(int dk, int dv) { return dk == DK && dv == DV; }
 
