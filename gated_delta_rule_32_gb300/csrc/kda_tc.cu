@@ -66,8 +66,8 @@ constexpr int R1_BYTES = 98304;
 constexpr int AKK_LD = 68;                        // fp32 row stride (floats)
 constexpr int OFF_AKK = OFF_R1;                   // [64][68] fp32   17408
 constexpr int OFF_TF = OFF_AKK + 17408;           // [64][68] fp32   17408
-constexpr int OFF_Y = OFF_TF + 17408;             // [3][16][17] fp32 3264 -> 4096
-constexpr int OFF_T = OFF_Y + 4096;               // T bf16 K-major   8192
+constexpr int OFF_Y = OFF_TF + 17408;             // [32][36] fp32    4608
+constexpr int OFF_T = OFF_Y + 4608;               // T bf16 K-major   8192
 constexpr int OFF_SB = OFF_T + 8192;              // S bf16 MN-major 16384
 constexpr int OFF_DL = OFF_SB + 16384;            // Delta bf16 MN    8192
 constexpr int OFF_X = OFF_DL + 8192;              // rows 0..63 of [-; A_qk]
@@ -246,6 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm100::tc_fence_after();
   };
 
+  const __nv_bfloat16* beta_g = static_cast<const __nv_bfloat16*>(p.beta);
+  float beta_next = 0.0f;  // beta of row `tid` of the next chunk
+  if (tid < C && nchunks > 0 && t0 + tid < t1)
+    beta_next = __bfloat162float(beta_g[(row_base + t0 + tid) * H + h]);
   if (tid == 0 && nchunks > 0) issue_tma(0);
   bool tma_pending = nchunks > 0;  // a load into the landing zone is in flight
   uint32_t tma_parity = 0;
@@ -260,12 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool dbg = dbg_nh && half == 0;
     const int64_t dbo = ci * C;  // debug row offset
 
-    // ---- (A) inputs of this chunk ------------------------------------------
+    // ---- (A) inputs of this chunk (beta was fetched one chunk ahead) -------
     if (tid < C) {
-      float b = 0.0f;
-      if (tid < L) b = __bfloat162float(
-          static_cast<const __nv_bfloat16*>(p.beta)[(row_base + cs + tid) * H + h]);
-      s_beta[tid] = b;
+      s_beta[tid] = beta_next;
+      beta_next = 0.0f;
+      if (ci + 1 < nchunks) {
+        const int64_t rn = cs + C + tid;
+        if (rn < t1) beta_next = __bfloat162float(beta_g[(row_base + rn) * H + h]);
+      }
     }
     {
       const bool ok = sm100::mbar_wait(bar_tma, (uint32_t)(ci & 1));
@@ -444,9 +450,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {       // beta_r A_kk row r, strict mask, fp32 for the solve
             const float br = s_beta[r];
-            float* row = s_akk + r * AKK_LD + 16 * b;
+            float4* row = reinterpret_cast<float4*>(s_akk + r * AKK_LD + 16 * b);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) row[c] = (16 * b + c < r) ? br * v[c] : 0.0f;
+            for (int c4 = 0; c4 < 4; ++c4) {
+              float t4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int c = 4 * c4 + e;
+                t4[e] = (16 * b + c < r) ? br * v[c] : 0.0f;
+              }
+              row[c4] = make_float4(t4[0], t4[1], t4[2], t4[3]);
+            }
           }
         }
       }
@@ -497,48 +511,91 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_parity = (uint32_t)((ci + 1) & 1);
     }
 
-    // ---- (E) T = (I + A_kk)^{-1}, fp32, blocked by 16 x 16 tiles -----------
-    if (tid < 64) {  // diagonal tiles: thread = (tile, column)
-      const int blk = tid >> 4, c = tid & 15;
+    // ---- (E) T = (I + A_kk)^{-1}, fp32 ------------------------------------
+    // (1) the four 16x16 diagonal tiles, one warp each, one column per lane,
+    //     right-looking substitution in registers (critical path: 15 FMAs);
+    // (2) T[2h+1, 2h] = -T[2h+1, 2h+1] A[2h+1, 2h] T[2h, 2h] for h = 0, 1;
+    // (3) T[H1, H0]  = -T[H1, H1] A[H1, H0] T[H0, H0] on the 32x32 halves.
+    // Upper triangles of the diagonal tiles are written as zeros in (1), so
+    // the products below may run over them; blocks above the block diagonal
+    // are never read.
+    if (warp < 4) {
+      const int blk = warp, c = lane & 15;
       const float* A = s_akk + (16 * blk) * AKK_LD + 16 * blk;
       float x[16];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float acc = (r == c) ? 1.0f : 0.0f;
-        if (r > c) {
+      for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.0f : 0.0f;
 #pragma unroll
-          for (int k2 = 0; k2 < 16; ++k2)
-            if (k2 >= c && k2 < r) acc = fmaf(-A[r * AKK_LD + k2], x[k2], acc);
-        }
-        x[r] = acc;
+      for (int i = 0; i < 15; ++i) {
+        const float xi = x[i];
+#pragma unroll
+        for (int r = i + 1; r < 16; ++r) x[r] = fmaf(-A[r * AKK_LD + i], xi, x[r]);
       }
+      if (lane < 16) {
 #pragma unroll
-      for (int r = 0; r < 16; ++r) s_tf[(16 * blk + r) * AKK_LD + 16 * blk + c] = x[r];
+        for (int r = 0; r < 16; ++r) s_tf[(16 * blk + r) * AKK_LD + 16 * blk + c] = x[r];
+      }
     }
     __syncthreads();
-#pragma unroll 1
-    for (int d = 1; d < 4; ++d) {
-      const int nblk = 4 - d;  // tiles (b + d, b), b = 0 .. nblk-1
-      // Y = A[a, b .. a-1] . T[b .. a-1, b]
-      for (int e = tid; e < nblk * 256; e += kThreads) {
-        const int b = e >> 8, r = (e >> 4) & 15, c = e & 15, a = b + d;
-        const float* Ar = s_akk + (16 * a + r) * AKK_LD;
-        float acc = 0.0f;
-        for (int k2 = 16 * b; k2 < 16 * a; ++k2)
-          acc = fmaf(Ar[k2], s_tf[k2 * AKK_LD + 16 * b + c], acc);
-        s_y[(b * 16 + r) * 17 + c] = acc;
+    {  // (2a) Y_h = A[2h+1, 2h] T[2h, 2h]: thread = (h, r, 2 columns)
+      const int hh = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
+      const int a1 = 2 * hh + 1, a0 = 2 * hh;
+      const float* Ar = s_akk + (16 * a1 + r) * AKK_LD + 16 * a0;
+      float y0 = 0.0f, y1 = 0.0f;
+#pragma unroll
+      for (int k2 = 0; k2 < 16; ++k2) {
+        const float av = Ar[k2];
+        const float2 tv = *reinterpret_cast<const float2*>(s_tf + (16 * a0 + k2) * AKK_LD + 16 * a0 + c0);
+        y0 = fmaf(av, tv.x, y0);
+        y1 = fmaf(av, tv.y, y1);
       }
-      __syncthreads();
-      // T[a, b] = -T[a, a] . Y
-      for (int e = tid; e < nblk * 256; e += kThreads) {
-        const int b = e >> 8, r = (e >> 4) & 15, c = e & 15, a = b + d;
-        const float* Tr = s_tf + (16 * a + r) * AKK_LD + 16 * a;
-        float acc = 0.0f;
-        for (int k2 = 0; k2 <= r; ++k2) acc = fmaf(Tr[k2], s_y[(b * 16 + k2) * 17 + c], acc);
-        s_tf[(16 * a + r) * AKK_LD + 16 * b + c] = -acc;
-      }
-      __syncthreads();
+      *reinterpret_cast<float2*>(s_y + (hh * 16 + r) * 36 + c0) = make_float2(y0, y1);
     }
+    __syncthreads();
+    {  // (2b) T[2h+1, 2h] = -T[2h+1, 2h+1] Y_h
+      const int hh = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
+      const int a1 = 2 * hh + 1, a0 = 2 * hh;
+      const float* Tr = s_tf + (16 * a1 + r) * AKK_LD + 16 * a1;
+      float y0 = 0.0f, y1 = 0.0f;
+#pragma unroll
+      for (int k2 = 0; k2 < 16; ++k2) {
+        if (k2 <= r) {
+          const float tv = Tr[k2];
+          const float2 yv = *reinterpret_cast<const float2*>(s_y + (hh * 16 + k2) * 36 + c0);
+          y0 = fmaf(tv, yv.x, y0);
+          y1 = fmaf(tv, yv.y, y1);
+        }
+      }
+      *reinterpret_cast<float2*>(s_tf + (16 * a1 + r) * AKK_LD + 16 * a0 + c0) = make_float2(-y0, -y1);
+    }
+    __syncthreads();
+    {  // (3a) Y = A[H1, H0] T[H0, H0]: thread = (row r of 32, 4 columns)
+      const int r = tid >> 3, c0 = (tid & 7) * 4;
+      const float* Ar = s_akk + (32 + r) * AKK_LD;
+      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k2 = c0; k2 < 32; ++k2) {
+        const float av = Ar[k2];
+        const float4 tv = *reinterpret_cast<const float4*>(s_tf + k2 * AKK_LD + c0);
+        y.x = fmaf(av, tv.x, y.x); y.y = fmaf(av, tv.y, y.y);
+        y.z = fmaf(av, tv.z, y.z); y.w = fmaf(av, tv.w, y.w);
+      }
+      *reinterpret_cast<float4*>(s_y + r * 36 + c0) = y;
+    }
+    __syncthreads();
+    {  // (3b) T[H1, H0] = -T[H1, H1] Y
+      const int r = tid >> 3, c0 = (tid & 7) * 4;
+      const float* Tr = s_tf + (32 + r) * AKK_LD + 32;
+      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k2 = 0; k2 <= r; ++k2) {
+        const float tv = Tr[k2];
+        const float4 yv = *reinterpret_cast<const float4*>(s_y + k2 * 36 + c0);
+        y.x = fmaf(tv, yv.x, y.x); y.y = fmaf(tv, yv.y, y.y);
+        y.z = fmaf(tv, yv.z, y.z); y.w = fmaf(tv, yv.w, y.w);
+      }
+      *reinterpret_cast<float4*>(s_tf + (32 + r) * AKK_LD + c0) =
+          make_float4(-y.x, -y.y, -y.z, -y.w);
+    }
+    __syncthreads();
     // T as bf16, K-major [r][i], unit diagonal, zero above
     for (int e = tid; e < 512; e += kThreads) {
       const int r = e >> 3, i0 = (e & 7) * 8;
