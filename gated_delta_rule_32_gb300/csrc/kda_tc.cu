@@ -56,11 +56,10 @@ constexpr int OFF_V = 49152;      // [64 rows][128 B] (this CTA's 64 value chann
 constexpr int R0_BYTES = 57344;
 // R1: Gram operands, then (after the Gram products) the per-chunk scratch
 constexpr int OFF_R1 = R0_BYTES;
-constexpr int OFF_AB0 = OFF_R1;               // A_0: 128 M-rows -> 32768
-constexpr int OFF_AB1 = OFF_AB0 + 32768;      // A_1:  96 M-rows -> 24576
-constexpr int OFF_AB2 = OFF_AB1 + 24576;      // A_2:  64 M-rows -> 16384
-constexpr int OFF_AB3 = OFF_AB2 + 16384;      // A_3:  32 M-rows ->  8192
-constexpr int OFF_KT = OFF_AB3 + 8192;        // Ktil: 4 blocks x 4096
+constexpr int OFF_A1 = OFF_R1;                // [q0; k0; q1; k1] MN-major 128 x 128  32768
+constexpr int OFF_B1 = OFF_A1 + 32768;        // [c0; c1]         MN-major  64 x 128  16384
+constexpr int OFF_A2 = OFF_B1 + 16384;        // [q1'; k1']       MN-major  64 x 128  16384
+constexpr int OFF_B2 = OFF_A2 + 16384;        // c0'              MN-major  32 x 128   8192
 constexpr int R1_BYTES = 98304;
 //   overlay after the Gram products:
 constexpr int AKK_LD = 68;                        // fp32 row stride (floats)
@@ -282,114 +281,124 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_pending = !ok;
       tma_parity = (uint32_t)(ci & 1);
     }
+    KDA_PHASE(11);
     __syncthreads();
     KDA_PHASE(0);
     if (*s_abort) break;
 
-    // ---- (B) gate: one key channel j, two tiles per thread ------------------
+    // ---- (B) gate: one key channel j, one half (two tiles) per thread -------
     {
-      const int j = tid & 127, pr = tid >> 7;  // tiles 2pr, 2pr+1
+      const int j = tid & 127, pr = tid >> 7;  // rows 32pr .. 32pr+31
       const unsigned char* sq = smem + OFF_Q + (j >> 6) * 8192;
       const unsigned char* sk = smem + OFF_K + (j >> 6) * 8192;
       const unsigned char* sg = smem + OFF_G + (j >> 6) * 8192;
       const int jc = j & 63;
-      float al[2][16];
+      // raw inputs of the 32 rows first (independent loads), then alpha
+      float qv[32], kv[32], al[32];
 #pragma unroll
-      for (int tt = 0; tt < 2; ++tt) {
-        const int a = 2 * pr + tt;
-        float prod = 1.0f;
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-          const int r = 16 * a + s;
-          const float x = ld_bf16(sg, sw128_off(r, jc));
-          const float av = (r < L) ? alpha_of(x) : 1.0f;
-          al[tt][s] = av;
-          prod *= av;
-        }
-        s_pt[a * 128 + j] = prod;
+      for (int s2 = 0; s2 < 32; ++s2) {
+        const int r = 32 * pr + s2;
+        const uint32_t o = sw128_off(r, jc);
+        const bool ok = r < L;
+        const float x = ld_bf16(sg, o);
+        qv[s2] = ok ? ld_bf16(sq, o) * p.scale : 0.0f;
+        kv[s2] = ok ? ld_bf16(sk, o) : 0.0f;
+        al[s2] = ok ? alpha_of(x) : 1.0f;
       }
+      float Pt0 = 1.0f, Pt1 = 1.0f;
+#pragma unroll
+      for (int s2 = 0; s2 < 16; ++s2) { Pt0 *= al[s2]; Pt1 *= al[16 + s2]; }
+      s_pt[(2 * pr) * 128 + j] = Pt0;
+      s_pt[(2 * pr + 1) * 128 + j] = Pt1;
       __syncthreads();
       const float P0 = s_pt[j], P1 = s_pt[128 + j], P2 = s_pt[256 + j], P3 = s_pt[384 + j];
-      const float Pv[4] = {P0, P1, P2, P3};
       if (pr == 0) s_gc[j] = P0 * P1 * P2 * P3;
+      // tile products are >= e^-80, so their inverses stay below e^80
+      const float invPa = __fdividef(1.0f, pr == 0 ? P0 : P2);   // first tile of the half
+      const float invPb = __fdividef(1.0f, pr == 0 ? P1 : P3);   // second tile
+      // per-tile constants (tt = 0, 1 for the two tiles of this half)
+      //   pre: gamma offset prod_{c<a} P_c;  post: Kdec offset prod_{c>a} P_c
+      const float pre0 = pr == 0 ? 1.0f : P0 * P1, pre1 = pr == 0 ? P0 : P0 * P1 * P2;
+      const float post0 = pr == 0 ? P1 * P2 * P3 : P3, post1 = pr == 0 ? P2 * P3 : 1.0f;
+      // E (within-tile prefix) and F (within-tile suffix) products
+      float E[32], F[32];
 #pragma unroll
       for (int tt = 0; tt < 2; ++tt) {
-        const int a = 2 * pr + tt;
-        float pre = 1.0f, post = 1.0f;
+        float e = 1.0f, f = 1.0f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (c < a) pre *= Pv[c];
-          if (c > a) post *= Pv[c];
+        for (int s2 = 0; s2 < 16; ++s2) { e *= al[16 * tt + s2]; E[16 * tt + s2] = e; }
+#pragma unroll
+        for (int s2 = 15; s2 >= 0; --s2) { F[16 * tt + s2] = f; f *= al[16 * tt + s2]; }
+      }
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {  // rows 8g8 .. 8g8+7 of the half
+        const int tt = g8 >> 1;
+        const int rr = 8 * g8;
+        float qE[8], kE[8], kF[8], t[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          qE[e] = qv[rr + e] * E[rr + e];
+          kE[e] = kv[rr + e] * E[rr + e];
+          kF[e] = kv[rr + e] * F[rr + e];
         }
-        float m[4];
+        // Gram operands of the two-level scheme (reference points: end of
+        // tile 0 for rows/columns of the first half, end of tile 2 for the
+        // second half, end of tile 1 for the cross block):
+        //   half 0: row e^{G_r - G_15}, col e^{G_15 - G_i}, cross col e^{G_31 - G_i}
+        //   half 1: row e^{G_r - G_47}, col e^{G_47 - G_i}, cross row e^{G_r - G_31}
+        // each a within-tile product times a per-tile constant, all within
+        // [e^-80, e^80] for the pairs that are kept.
+        const float rs = tt == 0 ? invPa : 1.0f;      // diagonal-half row factor
+        const float cs = tt == 0 ? 1.0f : invPb;      // diagonal-half column factor
+        if (pr == 0) {
+          const float csm = tt == 0 ? P1 : 1.0f;      // cross column factor
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          float mm = 1.0f;
+          for (int e = 0; e < 8; ++e) t[e] = qE[e] * rs;
+          st8_bf16(smem + OFF_A1 + mn_off(rr, j, 2048), t);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (c > b && c < a) mm *= Pv[c];
-          m[b] = (b == a) ? __fdividef(1.0f, Pv[a]) : mm;
+          for (int e = 0; e < 8; ++e) t[e] = kE[e] * rs;
+          st8_bf16(smem + OFF_A1 + mn_off(32 + rr, j, 2048), t);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t[e] = kF[e] * cs;
+          st8_bf16(smem + OFF_B1 + mn_off(rr, j, 1024), t);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t[e] = kF[e] * csm;
+          st8_bf16(smem + OFF_B2 + mn_off(rr, j, 512), t);
+        } else {
+          const float rsm = tt == 0 ? 1.0f : P2;      // cross row factor
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t[e] = qE[e] * rs;
+          st8_bf16(smem + OFF_A1 + mn_off(64 + rr, j, 2048), t);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t[e] = kE[e] * rs;
+          st8_bf16(smem + OFF_A1 + mn_off(96 + rr, j, 2048), t);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t[e] = qE[e] * rsm;
+          st8_bf16(smem + OFF_A2 + mn_off(rr, j, 1024), t);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t[e] = kE[e] * rsm;
+          st8_bf16(smem + OFF_A2 + mn_off(32 + rr, j, 1024), t);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) t[e] = kF[e] * cs;
+          st8_bf16(smem + OFF_B1 + mn_off(32 + rr, j, 1024), t);
         }
-        float E[16], F[16];
-        {
-          float e = 1.0f;
+        const float pre = tt == 0 ? pre0 : pre1, post = tt == 0 ? post0 : post1;
+        const int r0 = 32 * pr + rr;  // chunk row of this group
+        // Q gamma into rows 64.. of [W; Q gamma]
 #pragma unroll
-          for (int s = 0; s < 16; ++s) { e *= al[tt][s]; E[s] = e; }
-          float f = 1.0f;
+        for (int e = 0; e < 8; ++e) t[e] = qE[e] * pre;
+        st8_bf16(smem + OFF_WQ + mn_off(64 + r0, j, 2048), t);
+        // (beta K gamma)^T, K-major [j][r]
 #pragma unroll
-          for (int s = 15; s >= 0; --s) { F[s] = f; f *= al[tt][s]; }
-        }
+        for (int e = 0; e < 8; ++e) t[e] = s_beta[r0 + e] * kE[e] * pre;
+        st8_bf16(smem + OFF_BKG + k64_off(j, r0), t);
+        // (K e^{G_C - G})^T, K-major [j][r]
 #pragma unroll
-        for (int hg = 0; hg < 2; ++hg) {  // rows 8hg .. 8hg+7 of the tile
-          float qv[8], kv[8], bv[8];
+        for (int e = 0; e < 8; ++e) t[e] = kF[e] * post;
+        st8_bf16(smem + OFF_KD + k64_off(j, r0), t);
+        if (dbg && tp.dbg_gam) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int r = 16 * a + 8 * hg + e;
-            const bool ok = r < L;
-            qv[e] = ok ? ld_bf16(sq, sw128_off(r, jc)) * p.scale : 0.0f;
-            kv[e] = ok ? ld_bf16(sk, sw128_off(r, jc)) : 0.0f;
-            bv[e] = s_beta[r];
-          }
-          float t[8];
-          // Gram row operands for every column tile b <= a
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            if (b > a) continue;
-            const int Rb = 128 - 32 * b;
-            unsigned char* base = smem + OFF_AB0 + (b == 0 ? 0 : b == 1 ? 32768
-                                                               : b == 2 ? 57344 : 73728);
-            const uint32_t lbo = (uint32_t)Rb * 16u;
-            const int mq = 32 * (a - b) + 8 * hg;       // local M-row of q rows
-#pragma unroll
-            for (int e = 0; e < 8; ++e) t[e] = qv[e] * E[8 * hg + e] * m[b];
-            st8_bf16(base + mn_off(mq, j, lbo), t);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) t[e] = kv[e] * E[8 * hg + e] * m[b];
-            st8_bf16(base + mn_off(mq + 16, j, lbo), t);
-          }
-          // Ktil (B of the Gram product of column tile a): k F
-#pragma unroll
-          for (int e = 0; e < 8; ++e) t[e] = kv[e] * F[8 * hg + e];
-          st8_bf16(smem + OFF_KT + a * 4096 + mn_off(8 * hg, j, 256), t);
-          // Q gamma into rows 64.. of [W; Q gamma]
-#pragma unroll
-          for (int e = 0; e < 8; ++e) t[e] = qv[e] * E[8 * hg + e] * pre;
-          st8_bf16(smem + OFF_WQ + mn_off(64 + 16 * a + 8 * hg, j, 2048), t);
-          // (beta K gamma)^T, K-major [j][r]
-#pragma unroll
-          for (int e = 0; e < 8; ++e) t[e] = bv[e] * kv[e] * E[8 * hg + e] * pre;
-          st8_bf16(smem + OFF_BKG + k64_off(j, 16 * a + 8 * hg), t);
-          // (K e^{G_C - G})^T, K-major [j][r]
-#pragma unroll
-          for (int e = 0; e < 8; ++e) t[e] = kv[e] * F[8 * hg + e] * post;
-          st8_bf16(smem + OFF_KD + k64_off(j, 16 * a + 8 * hg), t);
-          if (dbg && tp.dbg_gam) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const int r = 16 * a + 8 * hg + e;
-              tp.dbg_gam[(dbo + r) * DK + j] = E[8 * hg + e] * pre;
-            }
-          }
+          for (int e = 0; e < 8; ++e) tp.dbg_gam[(dbo + r0 + e) * DK + j] = E[rr + e] * pre;
         }
       }
     }
@@ -397,22 +406,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     sync_all();
     KDA_PHASE(1);
 
-    // ---- (C) Gram products --------------------------------------------------
+    // ---- (C) Gram products: diagonal halves (M=128, N=64) and the cross
+    //      block (M=64, N=32), K = 128 key channels ---------------------------
     if (tid == 0) {
-      const uint32_t idesc = sm100::idesc_bf16(128, 16, 1, 1);
-      const uint32_t abase[4] = {0u, 32768u, 57344u, 73728u};
+      const uint32_t id1 = sm100::idesc_bf16(128, 64, 1, 1);
+      const uint32_t id2 = sm100::idesc_bf16(64, 32, 1, 1);
+      const uint32_t a1 = sm100::smem_u32(smem + OFF_A1), b1 = sm100::smem_u32(smem + OFF_B1);
+      const uint32_t a2 = sm100::smem_u32(smem + OFF_A2), b2 = sm100::smem_u32(smem + OFF_B2);
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint32_t lbo = (uint32_t)(128 - 32 * b) * 16u;
-        const uint32_t sa = sm100::smem_u32(smem + OFF_AB0 + abase[b]);
-        const uint32_t sb = sm100::smem_u32(smem + OFF_KT + b * 4096);
+      for (int s2 = 0; s2 < DK / 16; ++s2)
+        sm100::mma_ss(tmem + TM_G, sm100::smem_desc(a1 + s2 * 4096, 2048, 128),
+                      sm100::smem_desc(b1 + s2 * 2048, 1024, 128), id1, s2 > 0);
 #pragma unroll
-        for (int s = 0; s < DK / 16; ++s) {
-          const uint64_t ad = sm100::smem_desc(sa + s * 2 * lbo, lbo, 128);
-          const uint64_t bd = sm100::smem_desc(sb + s * 2 * 256, 256, 128);
-          sm100::mma_ss(tmem + TM_G + 16 * b, ad, bd, idesc, s > 0);
-        }
-      }
+      for (int s2 = 0; s2 < DK / 16; ++s2)
+        sm100::mma_ss(tmem + TM_G + 64, sm100::smem_desc(a2 + s2 * 2048, 1024, 128),
+                      sm100::smem_desc(b2 + s2 * 1024, 512, 128), id2, s2 > 0);
       commit_mma();
     }
     wait_mma();
@@ -421,46 +429,86 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- (D) Gram epilogue (warps 0-3) | S half and (beta V)^T (warps 4-7) --
     if (warp < 4) {
       const int l = tid;  // TMEM lane
-#pragma unroll 1
-      for (int b = 0; b < 4; ++b) {
-        float v[16];
-        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_G + 16 * b), v);
+      // diagonal halves: lane l holds row (l & 31) of q0 | k0 | q1 | k1
+      {
+        const int part = l >> 5, rl = l & 31;
+        const int hf = part >> 1, isk = part & 1;
+        const int r = 32 * hf + rl, cb = 32 * hf;  // row, first column of the block
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+          float w16[16];
+          sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_G + cb + c), w16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[c + e] = w16[e];
+        }
         sm100::tmem_wait_ld();
-        const int m = l + 32 * b;
-        if (m < 128) {
-          const int a = m >> 5, s = m & 31, r = 16 * a + (s & 15);
-          if (s < 16) {  // A_qk row r, columns of tile b, inclusive mask
-            float t[16];
+        if (!isk) {  // A_qk, inclusive mask; the block above the diagonal is zero
+          float t[8];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) t[c] = (16 * b + c <= r) ? v[c] : 0.0f;
-            unsigned char* base = smem + OFF_AQ;
-            st8_bf16(base + k64_off(r, 16 * b), t);
-            st8_bf16(base + k64_off(r, 16 * b + 8), t + 8);
-            if (b == a) {
-              const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-              for (int bb = a + 1; bb < 4; ++bb) {
-                st8_bf16(base + k64_off(r, 16 * bb), z);
-                st8_bf16(base + k64_off(r, 16 * bb + 8), z);
-              }
+          for (int g8 = 0; g8 < 4; ++g8) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t[e] = (cb + 8 * g8 + e <= r) ? v[8 * g8 + e] : 0.0f;
+            st8_bf16(smem + OFF_AQ + k64_off(r, cb + 8 * g8), t);
+          }
+          if (hf == 0) {
+            const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) st8_bf16(smem + OFF_AQ + k64_off(r, 32 + 8 * g8), z);
+          }
+          if (dbg && tp.dbg_aqk) {
+            for (int c = 0; c < 32; ++c)
+              tp.dbg_aqk[(dbo + r) * C + cb + c] = (cb + c <= r) ? v[c] : 0.0f;
+            if (hf == 0)
+              for (int c = 32; c < C; ++c) tp.dbg_aqk[(dbo + r) * C + c] = 0.0f;
+          }
+        } else {     // beta_r A_kk, strict mask, fp32 for the solve
+          const float br = s_beta[r];
+          float4* row = reinterpret_cast<float4*>(s_akk + r * AKK_LD + cb);
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            float t4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = 4 * c4 + e;
+              t4[e] = (cb + c < r) ? br * v[c] : 0.0f;
             }
-            if (dbg && tp.dbg_aqk) {
-              for (int c = 0; c < 16; ++c) tp.dbg_aqk[(dbo + r) * C + 16 * b + c] = t[c];
-              if (b == a)
-                for (int c = 16 * (a + 1); c < C; ++c) tp.dbg_aqk[(dbo + r) * C + c] = 0.0f;
+            row[c4] = make_float4(t4[0], t4[1], t4[2], t4[3]);
+          }
+        }
+      }
+      // cross block (rows 32..63 x columns 0..31) from the M = 64 product:
+      // product row m sits in lane 32 * (m / 16) + m % 16
+      {
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+          float w16[16];
+          sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_G + 64 + c), w16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[c + e] = w16[e];
+        }
+        sm100::tmem_wait_ld();
+        if ((l & 31) < 16) {
+          const int m = 16 * (l >> 5) + (l & 15);
+          const int r = 32 + (m & 31);
+          if (m < 32) {  // A_qk[r, 0..31]
+            float t[8];
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) t[e] = v[8 * g8 + e];
+              st8_bf16(smem + OFF_AQ + k64_off(r, 8 * g8), t);
             }
-          } else {       // beta_r A_kk row r, strict mask, fp32 for the solve
+            if (dbg && tp.dbg_aqk)
+              for (int c = 0; c < 32; ++c) tp.dbg_aqk[(dbo + r) * C + c] = v[c];
+          } else {       // beta_r A_kk[r, 0..31]
             const float br = s_beta[r];
-            float4* row = reinterpret_cast<float4*>(s_akk + r * AKK_LD + 16 * b);
+            float4* row = reinterpret_cast<float4*>(s_akk + r * AKK_LD);
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-              float t4[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int c = 4 * c4 + e;
-                t4[e] = (16 * b + c < r) ? br * v[c] : 0.0f;
-              }
-              row[c4] = make_float4(t4[0], t4[1], t4[2], t4[3]);
-            }
+            for (int c4 = 0; c4 < 8; ++c4)
+              row[c4] = make_float4(br * v[4 * c4], br * v[4 * c4 + 1], br * v[4 * c4 + 2],
+                                    br * v[4 * c4 + 3]);
           }
         }
       }
@@ -519,22 +567,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Upper triangles of the diagonal tiles are written as zeros in (1), so
     // the products below may run over them; blocks above the block diagonal
     // are never read.
-    if (warp < 4) {
-      const int blk = warp, c = lane & 15;
+    {  // (1) 8 warps: warp -> (tile, 8 columns); 4 lanes per column, lane q
+       //     owns rows q, q+4, q+8, q+12; the pivot x_i comes by shuffle
+      const int blk = warp >> 1, c = (warp & 1) * 8 + (lane >> 2), q = lane & 3;
       const float* A = s_akk + (16 * blk) * AKK_LD + 16 * blk;
-      float x[16];
+      float a_reg[4][16];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.0f : 0.0f;
+      for (int k4 = 0; k4 < 4; ++k4) {
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+          const float4 v4 = *reinterpret_cast<const float4*>(A + (4 * k4 + q) * AKK_LD + 4 * i4);
+          a_reg[k4][4 * i4] = v4.x; a_reg[k4][4 * i4 + 1] = v4.y;
+          a_reg[k4][4 * i4 + 2] = v4.z; a_reg[k4][4 * i4 + 3] = v4.w;
+        }
+      }
+      float x[4];
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) x[k4] = (4 * k4 + q == c) ? 1.0f : 0.0f;
+      const int src0 = lane & ~3;
 #pragma unroll
       for (int i = 0; i < 15; ++i) {
-        const float xi = x[i];
+        const float xi = __shfl_sync(0xffffffffu, x[i >> 2], src0 | (i & 3));
 #pragma unroll
-        for (int r = i + 1; r < 16; ++r) x[r] = fmaf(-A[r * AKK_LD + i], xi, x[r]);
+        for (int k4 = 0; k4 < 4; ++k4) {
+          if (4 * k4 + q > i) x[k4] = fmaf(-a_reg[k4][i], xi, x[k4]);
+        }
       }
-      if (lane < 16) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) s_tf[(16 * blk + r) * AKK_LD + 16 * blk + c] = x[r];
-      }
+      for (int k4 = 0; k4 < 4; ++k4)
+        s_tf[(16 * blk + 4 * k4 + q) * AKK_LD + 16 * blk + c] = x[k4];
     }
     __syncthreads();
     {  // (2a) Y_h = A[2h+1, 2h] T[2h, 2h]: thread = (h, r, 2 columns)
