@@ -216,6 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t nchunks = (t1 - t0 + C - 1) / C;
   uint32_t mma_phase = 0;
   bool mma_inflight = false;
+  bool tma_pending = nchunks > 0;  // a load into the landing zone is in flight
+  uint32_t tma_parity = 0;
   auto issue_tma = [&](int64_t ci) {
     const int row = (int)(row_base + t0 + ci * C);
     sm100::mbar_arrive_expect_tx(bar_tma, TX_BYTES);
@@ -245,14 +247,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm100::tc_fence_after();
   };
 
-  const __nv_bfloat16* beta_g = static_cast<const __nv_bfloat16*>(p.beta);
-  float beta_next = 0.0f;  // beta of row `tid` of the next chunk
-  if (tid < C && nchunks > 0 && t0 + tid < t1)
-    beta_next = __bfloat162float(beta_g[(row_base + t0 + tid) * H + h]);
+  // beta of row `tid` of the next chunk, kept as raw bf16 bits so that the
+  // load is only waited for one chunk later
+  const unsigned short* beta_g = static_cast<const unsigned short*>(p.beta);
+  unsigned short beta_next = 0;
+  if (tid < C && nchunks > 0 && t0 + tid < t1) beta_next = beta_g[(row_base + t0 + tid) * H + h];
   if (tid == 0 && nchunks > 0) issue_tma(0);
-  bool tma_pending = nchunks > 0;  // a load into the landing zone is in flight
-  uint32_t tma_parity = 0;
 
+  // decay factors alpha of this thread's 32 rows (key channel tid & 127,
+  // rows 32 * (tid >> 7) ..) for the chunk being prepared, and the tile
+  // products of those rows into s_pt
+  float al[32];
+  auto gate_alpha = [&](int64_t cj) {
+    const int j = tid & 127, pr = tid >> 7, jc = j & 63;
+    const int64_t csj = t0 + cj * C;
+    const int Lj = (t1 - csj) < C ? (int)(t1 - csj) : C;
+    const unsigned char* sg = smem + OFF_G + (j >> 6) * 8192;
+#pragma unroll
+    for (int s2 = 0; s2 < 32; ++s2) {
+      const int r = 32 * pr + s2;
+      al[s2] = (r < Lj) ? alpha_of(ld_bf16(sg, sw128_off(r, jc))) : 1.0f;
+    }
+    float Pt0 = 1.0f, Pt1 = 1.0f;
+#pragma unroll
+    for (int s2 = 0; s2 < 16; ++s2) { Pt0 *= al[s2]; Pt1 *= al[16 + s2]; }
+    s_pt[(2 * pr) * 128 + j] = Pt0;
+    s_pt[(2 * pr + 1) * 128 + j] = Pt1;
+  };
+  auto wait_tma = [&](int64_t cj) {
+    const bool ok = sm100::mbar_wait(bar_tma, (uint32_t)(cj & 1));
+    if (!ok) {
+      *s_abort = 1;
+      if (p.dev_status) atomicExch(p.dev_status, (int32_t)KDA_ERR_TIMEOUT);
+    }
+    tma_pending = !ok;
+    tma_parity = (uint32_t)(cj & 1);
+  };
 #ifdef KDA_PHASE_TIMING
   long long t_phase = clock64();
 #endif
@@ -265,21 +295,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- (A) inputs of this chunk (beta was fetched one chunk ahead) -------
     if (tid < C) {
-      s_beta[tid] = beta_next;
-      beta_next = 0.0f;
+      s_beta[tid] = __uint_as_float((uint32_t)beta_next << 16);  // bf16 bits -> fp32
+      beta_next = 0;
       if (ci + 1 < nchunks) {
         const int64_t rn = cs + C + tid;
-        if (rn < t1) beta_next = __bfloat162float(beta_g[(row_base + rn) * H + h]);
+        if (rn < t1) beta_next = beta_g[(row_base + rn) * H + h];
       }
     }
-    {
-      const bool ok = sm100::mbar_wait(bar_tma, (uint32_t)(ci & 1));
-      if (!ok) {
-        *s_abort = 1;
-        if (p.dev_status) atomicExch(p.dev_status, (int32_t)KDA_ERR_TIMEOUT);
-      }
-      tma_pending = !ok;
-      tma_parity = (uint32_t)(ci & 1);
+    if (ci == 0) {
+      wait_tma(0);
+      gate_alpha(0);  // later chunks: computed while the previous chunk's P runs
     }
     KDA_PHASE(11);
     __syncthreads();
@@ -291,26 +316,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = tid & 127, pr = tid >> 7;  // rows 32pr .. 32pr+31
       const unsigned char* sq = smem + OFF_Q + (j >> 6) * 8192;
       const unsigned char* sk = smem + OFF_K + (j >> 6) * 8192;
-      const unsigned char* sg = smem + OFF_G + (j >> 6) * 8192;
       const int jc = j & 63;
-      // raw inputs of the 32 rows first (independent loads), then alpha
-      float qv[32], kv[32], al[32];
+      // alpha of these rows and the tile products were computed earlier
+      // (gate_alpha); q and k of the 32 rows now
+      float qv[32], kv[32];
 #pragma unroll
       for (int s2 = 0; s2 < 32; ++s2) {
         const int r = 32 * pr + s2;
         const uint32_t o = sw128_off(r, jc);
         const bool ok = r < L;
-        const float x = ld_bf16(sg, o);
         qv[s2] = ok ? ld_bf16(sq, o) * p.scale : 0.0f;
         kv[s2] = ok ? ld_bf16(sk, o) : 0.0f;
-        al[s2] = ok ? alpha_of(x) : 1.0f;
       }
-      float Pt0 = 1.0f, Pt1 = 1.0f;
-#pragma unroll
-      for (int s2 = 0; s2 < 16; ++s2) { Pt0 *= al[s2]; Pt1 *= al[16 + s2]; }
-      s_pt[(2 * pr) * 128 + j] = Pt0;
-      s_pt[(2 * pr + 1) * 128 + j] = Pt1;
-      __syncthreads();
       const float P0 = s_pt[j], P1 = s_pt[128 + j], P2 = s_pt[256 + j], P3 = s_pt[384 + j];
       if (pr == 0) s_gc[j] = P0 * P1 * P2 * P3;
       // tile products are >= e^-80, so their inverses stay below e^80
@@ -634,11 +651,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = tid >> 3, c0 = (tid & 7) * 4;
       const float* Ar = s_akk + (32 + r) * AKK_LD;
       float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k2 = c0; k2 < 32; ++k2) {
-        const float av = Ar[k2];
-        const float4 tv = *reinterpret_cast<const float4*>(s_tf + k2 * AKK_LD + c0);
-        y.x = fmaf(av, tv.x, y.x); y.y = fmaf(av, tv.y, y.y);
-        y.z = fmaf(av, tv.z, y.z); y.w = fmaf(av, tv.w, y.w);
+#pragma unroll
+      for (int k2 = 0; k2 < 32; ++k2) {
+        if (k2 >= c0) {  // T[H0, H0] is lower triangular
+          const float av = Ar[k2];
+          const float4 tv = *reinterpret_cast<const float4*>(s_tf + k2 * AKK_LD + c0);
+          y.x = fmaf(av, tv.x, y.x); y.y = fmaf(av, tv.y, y.y);
+          y.z = fmaf(av, tv.z, y.z); y.w = fmaf(av, tv.w, y.w);
+        }
       }
       *reinterpret_cast<float4*>(s_y + r * 36 + c0) = y;
     }
@@ -647,11 +667,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int r = tid >> 3, c0 = (tid & 7) * 4;
       const float* Tr = s_tf + (32 + r) * AKK_LD + 32;
       float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int k2 = 0; k2 <= r; ++k2) {
-        const float tv = Tr[k2];
-        const float4 yv = *reinterpret_cast<const float4*>(s_y + k2 * 36 + c0);
-        y.x = fmaf(tv, yv.x, y.x); y.y = fmaf(tv, yv.y, y.y);
-        y.z = fmaf(tv, yv.z, y.z); y.w = fmaf(tv, yv.w, y.w);
+#pragma unroll
+      for (int k2 = 0; k2 < 32; ++k2) {
+        if (k2 <= r) {  // T[H1, H1] is lower triangular
+          const float tv = Tr[k2];
+          const float4 yv = *reinterpret_cast<const float4*>(s_y + k2 * 36 + c0);
+          y.x = fmaf(tv, yv.x, y.x); y.y = fmaf(tv, yv.y, y.y);
+          y.z = fmaf(tv, yv.z, y.z); y.w = fmaf(tv, yv.w, y.w);
+        }
       }
       *reinterpret_cast<float4*>(s_tf + (32 + r) * AKK_LD + c0) =
           make_float4(-y.x, -y.y, -y.z, -y.w);
@@ -737,6 +760,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm100::mma_ss(tmem + TM_P, sm100::smem_desc(sa + s * 4096, 2048, 128),
                       sm100::smem_desc(sb + s * 2048, 1024, 128), idesc, s > 0);
       commit_mma();
+    }
+    // the next chunk's tiles landed during this chunk: its decay factors are
+    // computed while the tensor cores work on P
+    if (ci + 1 < nchunks) {
+      wait_tma(ci + 1);
+      gate_alpha(ci + 1);
     }
     wait_mma();
     KDA_PHASE(7);
