@@ -95,7 +95,7 @@ constexpr uint32_t TX_BYTES = 57344;  // Q, K, G (2 boxes each) + V (1 box)
 
 #ifdef KDA_PHASE_TIMING
 // cycles spent in each phase of the chunk loop by thread 0 of CTA (0, 0, 0)
-__device__ unsigned long long kda_phase_cycles[16];
+__device__ unsigned long long kda_phase_cycles[24];
 #define KDA_PHASE(k)                                                           \
   do {                                                                         \
     if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {   \
@@ -145,9 +145,13 @@ struct TcParams {
 };
 
 __device__ __forceinline__ float alpha_of(float x) {
-  // exp(max(-softplus(x), -5)) = max(sigmoid(-x), e^-5)
-  const float e = __expf(x);
-  return fmaxf(__fdividef(1.0f, 1.0f + e), 0.006737946999085467f);
+  // exp(max(-softplus(x), -5)) = max(sigmoid(-x), e^-5) = max(1 / (1 + e^x), e^-5):
+  // one ex2 and one rcp on the special-function unit (flush-to-zero is exact
+  // here: e^x underflowing gives alpha = 1, overflowing gives the floor)
+  float t, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(x * 1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + t));
+  return fmaxf(r, 0.006737946999085467f);
 }
 
 // ---------------------------------------------------------------------------
@@ -166,7 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar_mma = bar_tma + 1;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   int* s_abort = reinterpret_cast<int*>(smem + OFF_MISC + 4);
-  float* s_beta = reinterpret_cast<float*>(smem + OFF_BETA);
+  unsigned short* s_beta_raw = reinterpret_cast<unsigned short*>(smem + OFF_BETA);
+  auto beta_at = [&](int r) { return __uint_as_float((uint32_t)s_beta_raw[r] << 16); };
   float* s_pt = reinterpret_cast<float*>(smem + OFF_PT);
   float* s_gc = reinterpret_cast<float*>(smem + OFF_GC);
   float* s_akk = reinterpret_cast<float*>(smem + OFF_AKK);
@@ -295,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- (A) inputs of this chunk (beta was fetched one chunk ahead) -------
     if (tid < C) {
-      s_beta[tid] = __uint_as_float((uint32_t)beta_next << 16);  // bf16 bits -> fp32
+      s_beta_raw[tid] = beta_next;  // bf16 bits; readers widen them
       beta_next = 0;
       if (ci + 1 < nchunks) {
         const int64_t rn = cs + C + tid;
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         st8_bf16(smem + OFF_WQ + mn_off(64 + r0, j, 2048), t);
         // (beta K gamma)^T, K-major [j][r]
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t[e] = s_beta[r0 + e] * kE[e] * pre;
+        for (int e = 0; e < 8; ++e) t[e] = beta_at(r0 + e) * kE[e] * pre;
         st8_bf16(smem + OFF_BKG + k64_off(j, r0), t);
         // (K e^{G_C - G})^T, K-major [j][r]
 #pragma unroll
@@ -443,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait_mma();
     KDA_PHASE(2);
 
-    // ---- (D) Gram epilogue (warps 0-3) | S half and (beta V)^T (warps 4-7) --
+    // ---- (D) Gram epilogue (warps 0-3) | (beta V)^T (warps 4-7) -------------
     if (warp < 4) {
       const int l = tid;  // TMEM lane
       // diagonal halves: lane l holds row (l & 31) of q0 | k0 | q1 | k1
@@ -480,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int c = 32; c < C; ++c) tp.dbg_aqk[(dbo + r) * C + c] = 0.0f;
           }
         } else {     // beta_r A_kk, strict mask, fp32 for the solve
-          const float br = s_beta[r];
+          const float br = beta_at(r);
           float4* row = reinterpret_cast<float4*>(s_akk + r * AKK_LD + cb);
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (dbg && tp.dbg_aqk)
               for (int c = 0; c < 32; ++c) tp.dbg_aqk[(dbo + r) * C + c] = v[c];
           } else {       // beta_r A_kk[r, 0..31]
-            const float br = s_beta[r];
+            const float br = beta_at(r);
             float4* row = reinterpret_cast<float4*>(s_akk + r * AKK_LD);
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
@@ -530,29 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      const int i = tid - 128;  // key channel = TMEM lane
-      float sv[64];
-#pragma unroll
-      for (int c = 0; c < 64; c += 16) {
-        float v[16];
-        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c), v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) sv[c + e] = v[e];
-      }
-      sm100::tmem_wait_ld();
-      // bf16 copy of S (B of the P product, MN-major: K = key channel i)
-#pragma unroll
-      for (int jg = 0; jg < 8; ++jg) st8_bf16(smem + OFF_SB + mn_off(8 * jg, i, 1024), sv + 8 * jg);
-      // S <- gamma_C * S ahead of the rank-64 update
-      const float gc = s_gc[i];
-#pragma unroll
-      for (int c = 0; c < 64; c += 16) {
-        uint32_t r[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(gc * sv[c + e]);
-        sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + c), r);
-      }
-      sm100::tmem_wait_st();
+      const int i = tid - 128;
       // (beta V)^T, K-major [value channel jv][row r]
       const int jv = i & 63, rh = i >> 6;  // rows 32rh .. 32rh+31
 #pragma unroll
@@ -561,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int r = 32 * rh + 8 * g8 + e;
-          t[e] = (r < L) ? s_beta[r] * ld_bf16(smem + OFF_V, sw128_off(r, jv)) : 0.0f;
+          t[e] = (r < L) ? beta_at(r) * ld_bf16(smem + OFF_V, sw128_off(r, jv)) : 0.0f;
         }
         st8_bf16(smem + OFF_BV + k64_off(jv, 32 * rh + 8 * g8), t);
       }
@@ -615,6 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         s_tf[(16 * blk + 4 * k4 + q) * AKK_LD + 16 * blk + c] = x[k4];
     }
     __syncthreads();
+    KDA_PHASE(15);
     {  // (2a) Y_h = A[2h+1, 2h] T[2h, 2h]: thread = (h, r, 2 columns)
       const int hh = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
       const int a1 = 2 * hh + 1, a0 = 2 * hh;
@@ -647,6 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<float2*>(s_tf + (16 * a1 + r) * AKK_LD + 16 * a0 + c0) = make_float2(-y0, -y1);
     }
     __syncthreads();
+    KDA_PHASE(16);
     {  // (3a) Y = A[H1, H0] T[H0, H0]: thread = (row r of 32, 4 columns)
       const int r = tid >> 3, c0 = (tid & 7) * 4;
       const float* Ar = s_akk + (32 + r) * AKK_LD;
@@ -663,6 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<float4*>(s_y + r * 36 + c0) = y;
     }
     __syncthreads();
+    KDA_PHASE(17);
     {  // (3b) T[H1, H0] = -T[H1, H1] Y
       const int r = tid >> 3, c0 = (tid & 7) * 4;
       const float* Tr = s_tf + (32 + r) * AKK_LD + 32;
@@ -680,6 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           make_float4(-y.x, -y.y, -y.z, -y.w);
     }
     __syncthreads();
+    KDA_PHASE(18);
     // T as bf16, K-major [r][i], unit diagonal, zero above
     for (int e = tid; e < 512; e += kThreads) {
       const int r = e >> 3, i0 = (e & 7) * 8;
@@ -717,6 +704,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                       sm100::smem_desc(s_bv + 256 * s, 128, 1024), idesc, s > 0);
       }
       commit_mma();
+    }
+    // while W^T and U are formed: bf16 copy of the entry state S (B of the
+    // P product) and S <- gamma_C * S ahead of the rank-64 update (warps
+    // 4-7, lane = key channel); neither touches what these products read
+    if (warp >= 4) {
+      const int i = tid - 128;
+      float sv[64];
+#pragma unroll
+      for (int c = 0; c < 64; c += 16) {
+        float v[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c), v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sv[c + e] = v[e];
+      }
+      sm100::tmem_wait_ld();
+#pragma unroll
+      for (int jg = 0; jg < 8; ++jg) st8_bf16(smem + OFF_SB + mn_off(8 * jg, i, 1024), sv + 8 * jg);
+      const float gc = s_gc[i];
+#pragma unroll
+      for (int c = 0; c < 64; c += 16) {
+        uint32_t r[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(gc * sv[c + e]);
+        sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + c), r);
+      }
+      sm100::tmem_wait_st();
     }
     wait_mma();
     KDA_PHASE(5);
@@ -764,8 +777,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the next chunk's tiles landed during this chunk: its decay factors are
     // computed while the tensor cores work on P
     if (ci + 1 < nchunks) {
+      KDA_PHASE(12);
       wait_tma(ci + 1);
+      KDA_PHASE(13);
       gate_alpha(ci + 1);
+      KDA_PHASE(14);
     }
     wait_mma();
     KDA_PHASE(7);
@@ -923,11 +939,11 @@ kda_status launch_tc(const TcParams& tp, cudaStream_t stream) {
 
 #ifdef KDA_PHASE_TIMING
 extern "C" int kda_phase_timing_read(unsigned long long* out16, int reset) {
-  if (cudaMemcpyFromSymbol(out16, kda_phase_cycles, sizeof(unsigned long long) * 16) !=
+  if (cudaMemcpyFromSymbol(out16, kda_phase_cycles, sizeof(unsigned long long) * 24) !=
       cudaSuccess)
     return -1;
   if (reset) {
-    unsigned long long z[16] = {0};
+    unsigned long long z[24] = {0};
     cudaMemcpyToSymbol(kda_phase_cycles, z, sizeof(z));
   }
   return 0;
