@@ -107,12 +107,46 @@ size_t kda_workspace_bytes(int N, int T, int H, int dk, int dv, int dtype, int c
   return 0;
 }
 
+static kda_status fwd_impl(const void* q, const void* k, const void* v, const void* g_logit,
+                           const void* beta, const float* init_state, void* out,
+                           float* final_state, int B, int T, int H, int dk, int dv,
+                           const int32_t* cu_seqlens, kda_dtype dtype, int chunk_size,
+                           float scale, int algo, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, float* ckpt, int ckpt_every, int ckpt_max,
+                           kda_stream_t stream_);
+
 kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, const void* g_logit,
                             const void* beta, const float* init_state, void* out,
                             float* final_state, int B, int T, int H, int dk, int dv,
                             const int32_t* cu_seqlens, kda_dtype dtype, int chunk_size,
                             float scale, int algo, void* workspace, size_t workspace_bytes,
                             int32_t* dev_status, kda_stream_t stream_) {
+  return fwd_impl(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk, dv,
+                  cu_seqlens, dtype, chunk_size, scale, algo, workspace, workspace_bytes,
+                  dev_status, nullptr, 0, 0, stream_);
+}
+
+kda_status kda_chunk_fwd_ckpt(const void* q, const void* k, const void* v, const void* g_logit,
+                              const void* beta, const float* init_state, void* out,
+                              float* final_state, int B, int T, int H, int dk, int dv,
+                              const int32_t* cu_seqlens, kda_dtype dtype, float scale,
+                              float* checkpoints, int every, int max_per_seq,
+                              int32_t* dev_status, kda_stream_t stream_) {
+  if (!checkpoints || every <= 0 || every % 64 != 0 || max_per_seq < 1)
+    return KDA_ERR_INVALID_ARG;
+  if (!aligned(checkpoints, 16)) return KDA_ERR_MISALIGNED;
+  return fwd_impl(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk, dv,
+                  cu_seqlens, dtype, 0, scale, KDA_ALGO_AUTO, nullptr, 0, dev_status,
+                  checkpoints, every, max_per_seq, stream_);
+}
+
+static kda_status fwd_impl(const void* q, const void* k, const void* v, const void* g_logit,
+                           const void* beta, const float* init_state, void* out,
+                           float* final_state, int B, int T, int H, int dk, int dv,
+                           const int32_t* cu_seqlens, kda_dtype dtype, int chunk_size,
+                           float scale, int algo, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, float* ckpt, int ckpt_every, int ckpt_max,
+                           kda_stream_t stream_) {
   kda_status st = check_args(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk,
                              dv, cu_seqlens, dtype, chunk_size, algo);
   if (st != KDA_OK) return st;
@@ -127,6 +161,7 @@ kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, const v
   p.init_state = init_state; p.out = out; p.final_state = final_state;
   p.cu_seqlens = cu_seqlens; p.dev_status = dev_status;
   p.N = B; p.T = T; p.H = H; p.dk = dk; p.dv = dv; p.scale = scale;
+  p.ckpt = ckpt; p.ckpt_every = ckpt_every; p.ckpt_max = ckpt_max;
   if (algo == KDA_ALGO_TC && !use_tc(dtype, dk, dv, chunk_size, algo))
     return KDA_ERR_UNSUPPORTED;
   if (use_tc(dtype, dk, dv, chunk_size, algo)) return kda_launch_tc(p, stream);

@@ -28,6 +28,9 @@ struct FwdParams {
   float* final_state;
   const int32_t* cu_seqlens;  // device, may be null
   int32_t* dev_status;        // device, may be null
+  float* ckpt;                // device, may be null: state checkpoints
+  int ckpt_every;             // tokens between checkpoints (multiple of 64)
+  int ckpt_max;               // checkpoint slots per (sequence, head)
   int N;                      // number of sequences
   int T;                      // tokens per batch row (packed: total)
   int H, dk, dv;

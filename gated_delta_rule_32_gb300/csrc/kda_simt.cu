@@ -187,6 +187,15 @@ __global__ void __launch_bounds__(NT) kda_simt_kernel(kda::FwdParams p) {
 #pragma unroll
       for (int r = 0; r < C; ++r) acc = fmaf(sm.Kd[r][j], sm.D[r][c], acc);
       sm.S[j][c] = acc;
+      // state checkpoint after every `ckpt_every` tokens of the sequence
+      if (p.ckpt) {
+        const int64_t done = cs + L - t0;
+        if (L == C && done % p.ckpt_every == 0) {
+          const int64_t slot = done / p.ckpt_every - 1;
+          if (slot < p.ckpt_max)
+            p.ckpt[((((int64_t)n * H + h) * p.ckpt_max + slot) * DK + j) * dv + c0 + c] = acc;
+        }
+      }
     }
   }
   __syncthreads();

@@ -299,14 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t dbo = ci * C;  // debug row offset
 
     // ---- (A) inputs of this chunk (beta was fetched one chunk ahead) -------
-    if (tid < C) {
-      s_beta_raw[tid] = beta_next;  // bf16 bits; readers widen them
-      beta_next = 0;
-      if (ci + 1 < nchunks) {
-        const int64_t rn = cs + C + tid;
-        if (rn < t1) beta_next = beta_g[(row_base + rn) * H + h];
-      }
-    }
+    if (tid < C) s_beta_raw[tid] = beta_next;  // bf16 bits; readers widen them
     if (ci == 0) {
       wait_tma(0);
       gate_alpha(0);  // later chunks: computed while the previous chunk's P runs
@@ -782,6 +775,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       KDA_PHASE(13);
       gate_alpha(ci + 1);
       KDA_PHASE(14);
+      // beta of the next chunk, stored at its start
+      if (tid < C) {
+        const int64_t rn = cs + C + tid;
+        beta_next = (rn < t1) ? beta_g[(row_base + rn) * H + h] : (unsigned short)0;
+      }
     }
     wait_mma();
     KDA_PHASE(7);
@@ -825,6 +823,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     wait_mma();
     KDA_PHASE(9);
 
+    // ---- (K') state checkpoint (warps 4-7, lane = key channel) ------------
+    if (p.ckpt && warp >= 4 && L == C) {
+      const int64_t done = cs + L - t0;
+      if (done % p.ckpt_every == 0 && done / p.ckpt_every <= p.ckpt_max) {
+        const int i = tid - 128;
+        float* dst = p.ckpt + ((((int64_t)n * H + h) * p.ckpt_max + done / p.ckpt_every - 1) *
+                                   DK + i) * DV + half * DVH;
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) {
+          float v[16];
+          sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c), v);
+          sm100::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(dst + c + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+      }
+    }
     // ---- (K) output rows (warps 2-3, lanes 64..127 = row r) ------------------
     if (warp == 2 || warp == 3) {
       const int r = tid - 64;
@@ -977,6 +993,7 @@ extern "C" kda_status kda_debug_intra(const uint16_t* q, const uint16_t* k, cons
   TcParams tp;
   tp.p.q = q; tp.p.k = k; tp.p.v = v; tp.p.g = g_logit; tp.p.beta = beta;
   tp.p.init_state = nullptr; tp.p.out = out; tp.p.final_state = nullptr;
+  tp.p.ckpt = nullptr; tp.p.ckpt_every = 0; tp.p.ckpt_max = 0;
   tp.p.cu_seqlens = cu_seqlens; tp.p.dev_status = nullptr;
   tp.p.N = B; tp.p.T = T; tp.p.H = H; tp.p.dk = dk; tp.p.dv = dv; tp.p.scale = 1.0f;
   tp.dbg_n = n; tp.dbg_h = h;

@@ -44,6 +44,9 @@ _SIGS = {
     "kda_chunk_fwd_ex": (_i, [_vp] * 8 + [_i] * 5 + [_vp, _i, _i, ctypes.c_float, _i, _vp,
                                                    ctypes.c_size_t, _vp, _vp]),
     "kda_workspace_bytes": (ctypes.c_size_t, [_i] * 9),
+    "kda_decode": (_i, [_vp] * 7 + [_i] * 6 + [ctypes.c_float, _vp]),
+    "kda_chunk_fwd_ckpt": (_i, [_vp] * 8 + [_i] * 5 + [_vp, _i, ctypes.c_float, _vp, _i, _i,
+                                                     _vp, _vp]),
     "kda_chunk_fwd_host": (_i, [_vp] * 8 + [_i] * 5 + [_vp, _i, ctypes.c_float, _vp,
                                                    ctypes.c_size_t, _vp]),
     "kda_host_staging_bytes": (ctypes.c_size_t, [_i] * 9),
@@ -134,6 +137,21 @@ def kda_chunk_fwd_ex(q, k, v, g_logit, beta, init_state, out, final_state, B, T,
                                    _p(out), _p(final_state), B, T, H, dk, dv, _p(cu_seqlens),
                                    dtype, chunk_size, float(scale), algo, _p(workspace),
                                    workspace_bytes, _p(dev_status), _stream(stream))
+
+
+def kda_chunk_fwd_ckpt(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk, dv,
+                       cu_seqlens=None, dtype=KDA_BF16, scale=1.0, checkpoints=None, every=512,
+                       max_per_seq=1, dev_status=None, stream=None) -> int:
+    return load().kda_chunk_fwd_ckpt(_p(q), _p(k), _p(v), _p(g_logit), _p(beta),
+                                     _p(init_state), _p(out), _p(final_state), B, T, H, dk, dv,
+                                     _p(cu_seqlens), dtype, float(scale), _p(checkpoints),
+                                     every, max_per_seq, _p(dev_status), _stream(stream))
+
+
+def kda_decode(q, k, v, g_logit, beta, state, out, N, T, H, dk, dv, dtype=KDA_BF16, scale=1.0,
+               stream=None) -> int:
+    return load().kda_decode(_p(q), _p(k), _p(v), _p(g_logit), _p(beta), _p(state), _p(out), N,
+                             T, H, dk, dv, dtype, float(scale), _stream(stream))
 
 
 def kda_workspace_bytes(N, T, H, dk, dv, dtype=KDA_BF16, chunk_size=0, algo=KDA_ALGO_AUTO,

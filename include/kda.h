@@ -126,6 +126,38 @@ kda_status kda_chunk_fwd_ex(const void* q, const void* k, const void* v, const v
                             float scale, int algo, void* workspace, size_t workspace_bytes,
                             int32_t* dev_status, kda_stream_t stream);
 
+/*
+ * kda_chunk_fwd_ckpt -- kda_chunk_fwd_ex (automatic path, default chunk)
+ * that also writes state checkpoints: after every `every` tokens of each
+ * sequence (every: a multiple of 64), the state S at that point goes to
+ * checkpoints[n][h][c][dk][dv] (fp32, device, 16-byte aligned), c = 0 ..
+ * max_per_seq-1 counting boundaries from the sequence start; boundaries
+ * beyond max_per_seq are not written, nor are slots of a sequence that
+ * ends before them.  The state at a checkpoint is what a later call would
+ * take as init_state to resume there: the recurrent half of the prefix
+ * cache, checkpointed on a sparse subset of hash boundaries (Kimi K3
+ * architecture, orkas.ai, "The cost is paid in the serving stack").
+ */
+kda_status kda_chunk_fwd_ckpt(const void* q, const void* k, const void* v, const void* g_logit,
+                              const void* beta, const float* init_state, void* out,
+                              float* final_state, int B, int T, int H, int dk, int dv,
+                              const int32_t* cu_seqlens, kda_dtype dtype, float scale,
+                              float* checkpoints, int every, int max_per_seq,
+                              int32_t* dev_status, kda_stream_t stream);
+
+/*
+ * kda_decode -- the recurrent form for a few tokens per sequence (a decode
+ * step, or the speculative-decoding rebuild that replays accepted tokens'
+ * cached projected inputs from a saved state): the same operation as
+ * kda_chunk_fwd_ex with init_state == final_state == `state`, computed
+ * token by token with the state slice held on chip, for short T.
+ * Dense layouts [N, T, H, .]; `state` [N, H, dk, dv] fp32, read and
+ * updated in place.  dtype KDA_BF16 or KDA_F32; dk, dv in {16, 32, 64, 128}.
+ */
+kda_status kda_decode(const void* q, const void* k, const void* v, const void* g_logit,
+                      const void* beta, float* state, void* out, int N, int T, int H, int dk,
+                      int dv, kda_dtype dtype, float scale, kda_stream_t stream);
+
 /* Device scratch bytes kda_chunk_fwd_ex needs for these sizes (0 = none).
  * N = number of sequences (B, or the cu_seqlens count when packed). */
 size_t kda_workspace_bytes(int N, int T, int H, int dk, int dv, int dtype, int chunk_size,
