@@ -62,6 +62,29 @@ kda_status check_args(const void* q, const void* k, const void* v, const void* g
   return KDA_OK;
 }
 
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      n = 148;
+  }
+  return n;
+}
+
+// Segments per sequence for the tensor-core path: only dense batches whose
+// (sequence, head) chains would leave more than half of the SMs idle, with
+// segments of at least 1024 tokens.
+int auto_segments(int B, int T, int H, int sms) {
+  const int ctas = B * H * 2;  // two CTAs (value halves) per chain
+  if (ctas * 2 > sms || T < 2048) return 1;
+  int nseg = sms / ctas;
+  const int by_len = T / 1024;
+  if (nseg > by_len) nseg = by_len;
+  return nseg < 2 ? 1 : nseg;
+}
+
 bool use_tc(int dtype, int dk, int dv, int chunk_size, int algo) {
   if (algo == KDA_ALGO_SIMT) return false;
   if (dtype != KDA_BF16 || chunk_size == 16) return false;
@@ -69,6 +92,25 @@ bool use_tc(int dtype, int dk, int dv, int chunk_size, int algo) {
 }
 
 }  // namespace
+
+kda_status kda_run_segmented(const kda::FwdParams& p, int nseg, void* scratch,
+                             cudaStream_t stream);
+size_t kda_seg_scratch_bytes(int N, int H, int nseg, int dk, int dv);
+
+static kda_status run_segmented_ws(const kda::FwdParams& p, int nseg, void* workspace,
+                                   size_t workspace_bytes, cudaStream_t stream) {
+  const size_t need = kda_seg_scratch_bytes(p.N, p.H, nseg, p.dk, p.dv);
+  if (workspace) {
+    if (workspace_bytes < need) return KDA_ERR_WORKSPACE;
+    if (((uintptr_t)workspace & 255) != 0) return KDA_ERR_MISALIGNED;
+    return kda_run_segmented(p, nseg, workspace, stream);
+  }
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  kda_status st = kda_run_segmented(p, nseg, ws, stream);
+  if (cudaFreeAsync(ws, stream) != cudaSuccess && st == KDA_OK) st = KDA_ERR_CUDA;
+  return st;
+}
 
 extern "C" {
 
@@ -102,9 +144,10 @@ int kda_resolve_algo(int dtype, int dk, int dv, int chunk_size, int algo) {
 
 size_t kda_workspace_bytes(int N, int T, int H, int dk, int dv, int dtype, int chunk_size,
                            int algo, int packed) {
-  (void)N; (void)T; (void)H; (void)dk; (void)dv; (void)dtype; (void)chunk_size; (void)algo;
-  (void)packed;
-  return 0;
+  if (packed || N < 1 || H < 1 || T < 1) return 0;
+  if (!use_tc(dtype, dk, dv, chunk_size, algo)) return 0;
+  const int nseg = auto_segments(N, T, H, sm_count());
+  return nseg > 1 ? kda_seg_scratch_bytes(N, H, nseg, dk, dv) : 0;
 }
 
 static kda_status fwd_impl(const void* q, const void* k, const void* v, const void* g_logit,
@@ -156,7 +199,7 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const vo
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), stream) != cudaSuccess)
     return KDA_ERR_CUDA;
-  kda::FwdParams p;
+  kda::FwdParams p{};
   p.q = q; p.k = k; p.v = v; p.g = g_logit; p.beta = beta;
   p.init_state = init_state; p.out = out; p.final_state = final_state;
   p.cu_seqlens = cu_seqlens; p.dev_status = dev_status;
@@ -164,8 +207,38 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const vo
   p.ckpt = ckpt; p.ckpt_every = ckpt_every; p.ckpt_max = ckpt_max;
   if (algo == KDA_ALGO_TC && !use_tc(dtype, dk, dv, chunk_size, algo))
     return KDA_ERR_UNSUPPORTED;
-  if (use_tc(dtype, dk, dv, chunk_size, algo)) return kda_launch_tc(p, stream);
-  return kda_launch_simt(p, dtype, stream);
+  if (!use_tc(dtype, dk, dv, chunk_size, algo)) return kda_launch_simt(p, dtype, stream);
+  const int nseg = (cu_seqlens || ckpt) ? 1 : auto_segments(B, T, H, sm_count());
+  if (nseg <= 1) return kda_launch_tc(p, stream);
+  return run_segmented_ws(p, nseg, workspace, workspace_bytes, stream);
+}
+
+kda_status kda_chunk_fwd_seg(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                             const uint16_t* g_logit, const uint16_t* beta,
+                             const float* init_state, uint16_t* out, float* final_state, int B,
+                             int T, int H, int dk, int dv, float scale, int nseg,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             kda_stream_t stream_) {
+  kda_status st = check_args(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk,
+                             dv, nullptr, KDA_BF16, 0, KDA_ALGO_TC);
+  if (st != KDA_OK) return st;
+  if (!kda_tc_supported(dk, dv)) return KDA_ERR_UNSUPPORTED;
+  if (nseg < 1 || nseg > 4096) return KDA_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), stream) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  kda::FwdParams p{};
+  p.q = q; p.k = k; p.v = v; p.g = g_logit; p.beta = beta;
+  p.init_state = init_state; p.out = out; p.final_state = final_state;
+  p.dev_status = dev_status;
+  p.N = B; p.T = T; p.H = H; p.dk = dk; p.dv = dv; p.scale = scale;
+  if (nseg == 1 || T == 0) return kda_launch_tc(p, stream);
+  return run_segmented_ws(p, nseg, workspace, workspace_bytes, stream);
+}
+
+size_t kda_seg_workspace_bytes(int B, int H, int nseg, int dk, int dv) {
+  if (B < 1 || H < 1 || nseg < 2) return 0;
+  return kda_seg_scratch_bytes(B, H, nseg, dk, dv);
 }
 
 kda_status kda_chunk_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v,

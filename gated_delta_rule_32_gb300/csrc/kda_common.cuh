@@ -28,6 +28,13 @@ struct FwdParams {
   float* final_state;
   const int32_t* cu_seqlens;  // device, may be null
   int32_t* dev_status;        // device, may be null
+  // segments (dense batches only): sequence n is cut into nseg pieces of
+  // seglen tokens (a multiple of 64) that run as independent chains
+  int nseg;                   // 0 or 1: no segmentation
+  int64_t seglen;
+  const float* seg_init;      // [N][nseg][H][dk][dv] entry states of segments
+  float* seg_final;           // [N][nseg][H][dk][dv] zero-start final states
+  float* seg_P;               // [N][nseg][H][dk][dk] cumulative transitions
   float* ckpt;                // device, may be null: state checkpoints
   int ckpt_every;             // tokens between checkpoints (multiple of 64)
   int ckpt_max;               // checkpoint slots per (sequence, head)
@@ -83,4 +90,6 @@ __device__ __forceinline__ bool seq_span(const FwdParams& p, int n, int64_t& row
 // Launchers (one per translation unit).
 kda_status kda_launch_simt(const kda::FwdParams& p, kda_dtype dtype, cudaStream_t stream);
 kda_status kda_launch_tc(const kda::FwdParams& p, cudaStream_t stream);
+kda_status kda_launch_tc_summary(const kda::FwdParams& p, cudaStream_t stream);
+kda_status kda_launch_seg_scan(const kda::FwdParams& p, cudaStream_t stream);
 bool kda_tc_supported(int dk, int dv);

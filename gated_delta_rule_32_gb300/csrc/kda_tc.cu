@@ -67,28 +67,40 @@ constexpr int OFF_AKK = OFF_R1;                   // [64][68] fp32   17408
 constexpr int OFF_TF = OFF_AKK + 17408;           // [64][68] fp32   17408
 constexpr int OFF_Y = OFF_TF + 17408;             // [32][36] fp32    4608
 constexpr int OFF_T = OFF_Y + 4608;               // T bf16 K-major   8192
-constexpr int OFF_SB = OFF_T + 8192;              // S bf16 MN-major 16384
-constexpr int OFF_DL = OFF_SB + 16384;            // Delta bf16 MN    8192
-constexpr int OFF_X = OFF_DL + 8192;              // rows 0..63 of [-; A_qk]
-constexpr int OFF_AQ = OFF_X + 8192;              // A_qk masked bf16 8192
-constexpr int OFF_BV = OFF_AQ + 8192;             // (beta V)^T bf16  8192
-static_assert(OFF_BV + 8192 <= OFF_R1 + R1_BYTES, "R1 overlay");
-// R2: [W; Q gamma] MN-major, 128 M-rows x 128 K
-constexpr int OFF_WQ = OFF_R1 + R1_BYTES;
-// R3: (beta K gamma)^T and (K dec)^T, K-major 128 x 64
-constexpr int OFF_BKG = OFF_WQ + 32768;
-constexpr int OFF_KD = OFF_BKG + 16384;
-// small
-constexpr int OFF_BETA = OFF_KD + 16384;          // 64 fp32
-constexpr int OFF_PT = OFF_BETA + 256;            // [4][128] fp32 tile products
-constexpr int OFF_GC = OFF_PT + 2048;             // [128] fp32 gamma_C
-constexpr int OFF_BAR = OFF_GC + 512;             // mbarriers
-constexpr int OFF_MISC = OFF_BAR + 64;            // tmem base, abort flag
-constexpr int SMEM_BYTES = OFF_MISC + 64;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-// TMEM columns
-constexpr uint32_t TM_S = 0, TM_P = 64, TM_U = 128, TM_W = 192, TM_G = 256;
+// The rest of the map depends on the kernel mode: MODE 0 is the forward
+// (state half: 64 value columns); MODE 1 is the segment summary, which
+// carries the zero-start state half next to 64 columns of the segment's
+// cumulative transition P (dk x dk), i.e. 128 state columns, and writes no
+// output.  Lay<MODE> gives the offsets.
+template <int MODE>
+struct Lay {
+  static constexpr int SC = MODE == 0 ? 64 : 128;          // state columns in TMEM
+  static constexpr int OFF_SB = OFF_T + 8192;             // [S | P] bf16, MN-major 128 x SC
+  static constexpr int OFF_DL = OFF_SB + SC * 256;         // Delta bf16, MN-major 64 x SC
+  static constexpr int OFF_X = OFF_DL + SC * 128;          // rows 0..63 of [-; A_qk] (MODE 0)
+  static constexpr int OFF_AQ = OFF_X + 8192;              // A_qk masked bf16     (MODE 0)
+  static constexpr int OFF_BV = MODE == 0 ? OFF_AQ + 8192 : OFF_X;  // (beta V)^T bf16 8192
+  static constexpr int R1_BYTES_M = MODE == 0 ? R1_BYTES : OFF_BV + 8192 - OFF_R1;
+  // R2: [W; Q gamma] MN-major, 128 M-rows x 128 K
+  static constexpr int OFF_WQ = OFF_R1 + R1_BYTES_M;
+  // R3: (beta K gamma)^T and (K dec)^T, K-major 128 x 64
+  static constexpr int OFF_BKG = OFF_WQ + 32768;
+  static constexpr int OFF_KD = OFF_BKG + 16384;
+  // small
+  static constexpr int OFF_BETA = OFF_KD + 16384;          // 64 bf16
+  static constexpr int OFF_PT = OFF_BETA + 256;            // [4][128] fp32 tile products
+  static constexpr int OFF_GC = OFF_PT + 2048;             // [128] fp32 gamma_C
+  static constexpr int OFF_BAR = OFF_GC + 512;             // mbarriers
+  static constexpr int OFF_MISC = OFF_BAR + 64;            // tmem base, abort flag
+  static constexpr int SMEM_BYTES = OFF_MISC + 64;
+  // TMEM columns
+  static constexpr uint32_t TM_S = 0, TM_P = SC, TM_U = 2 * SC, TM_W = 2 * SC + 64,
+                            TM_G = 2 * SC + 128;
+};
+static_assert(Lay<0>::OFF_BV + 8192 <= OFF_R1 + R1_BYTES, "R1 overlay");
+static_assert(Lay<0>::SMEM_BYTES <= 232448 && Lay<1>::SMEM_BYTES <= 232448, "shared memory");
+static_assert(Lay<1>::TM_G + 96 <= 512, "tensor memory");
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t TX_BYTES = 57344;  // Q, K, G (2 boxes each) + V (1 box)
@@ -155,15 +167,26 @@ __device__ __forceinline__ float alpha_of(float x) {
 }
 
 // ---------------------------------------------------------------------------
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_g,
                         const __grid_constant__ CUtensorMap tm_v, const TcParams tp) {
   extern __shared__ __align__(1024) unsigned char smem[];
+  using Ly = Lay<MODE>;
+  constexpr int SC = Ly::SC;
+  constexpr int OFF_SB = Ly::OFF_SB, OFF_DL = Ly::OFF_DL, OFF_X = Ly::OFF_X, OFF_AQ = Ly::OFF_AQ;
+  constexpr int OFF_BV = Ly::OFF_BV, OFF_WQ = Ly::OFF_WQ, OFF_BKG = Ly::OFF_BKG;
+  constexpr int OFF_KD = Ly::OFF_KD, OFF_BETA = Ly::OFF_BETA, OFF_PT = Ly::OFF_PT;
+  constexpr int OFF_GC = Ly::OFF_GC, OFF_BAR = Ly::OFF_BAR, OFF_MISC = Ly::OFF_MISC;
+  constexpr uint32_t TM_S = Ly::TM_S, TM_P = Ly::TM_P, TM_U = Ly::TM_U, TM_W = Ly::TM_W;
+  constexpr uint32_t TM_G = Ly::TM_G;
   const kda::FwdParams& p = tp.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int half = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+  const int half = blockIdx.x, h = blockIdx.y;
+  const int nseg = p.nseg > 1 ? p.nseg : 1;
+  const int n = (int)blockIdx.z / nseg, sg = (int)blockIdx.z % nseg;  // sequence, segment
   const int H = p.H;
 
   uint64_t* bar_tma = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -180,6 +203,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int64_t row_base, t0, t1;
   if (!kda::seq_span(p, n, row_base, t0, t1)) return;  // uniform over the CTA
+  if (nseg > 1) {  // this CTA's segment [t0 + sg * seglen, ...) of the sequence
+    const int64_t a = t0 + (int64_t)sg * p.seglen;
+    const int64_t b = a + p.seglen;
+    t0 = a < t1 ? a : t1;
+    t1 = b < t1 ? b : t1;
+  }
 
   if (warp == 0) {
     sm100::tmem_alloc(s_tmem, TM_COLS);
@@ -203,16 +232,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_q = 32u * (warp & 3);  // this warp's TMEM lane quarter
   const int64_t sbase = ((int64_t)n * H + h) * (int64_t)DK * DV + half * DVH;
+  // segment-indexed state slot [n][sg][h] of the segment scratch
+  const int64_t segbase = (((int64_t)n * nseg + sg) * H + h) * (int64_t)DK * DV + half * DVH;
 
-  // ---- initial state half into TMEM (lane = key channel) -------------------
+  // ---- initial state into TMEM (lane = key channel) ------------------------
+  //   MODE 0: init_state (first segment) or the segment's resolved entry
+  //   state; MODE 1: zero state and, in columns 64.., this half's columns of
+  //   the identity (the transition of an empty prefix)
   if (warp < 4) {
     const int i = warp * 32 + lane;
-    for (int c = 0; c < DVH; c += 16) {
+    const float* src = nullptr;
+    int64_t base = 0;
+    if (MODE == 0) {
+      if (sg == 0) { src = p.init_state; base = sbase; }
+      else { src = p.seg_init; base = segbase; }
+    }
+    for (int c = 0; c < SC; c += 16) {
       uint32_t r[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        r[e] = __float_as_uint(p.init_state ? p.init_state[sbase + (int64_t)i * DV + c + e]
-                                            : 0.0f);
+      for (int e = 0; e < 16; ++e) {
+        float x = 0.0f;
+        if (MODE == 0) {
+          if (src) x = src[base + (int64_t)i * DV + c + e];
+        } else if (c >= 64) {
+          x = (i == half * 64 + (c - 64) + e) ? 1.0f : 0.0f;
+        }
+        r[e] = __float_as_uint(x);
+      }
       sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + c), r);
     }
     sm100::tmem_wait_st();
@@ -399,10 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float pre = tt == 0 ? pre0 : pre1, post = tt == 0 ? post0 : post1;
         const int r0 = 32 * pr + rr;  // chunk row of this group
-        // Q gamma into rows 64.. of [W; Q gamma]
+        // Q gamma into rows 64.. of [W; Q gamma] (the output needs it)
+        if (MODE == 0) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t[e] = qE[e] * pre;
-        st8_bf16(smem + OFF_WQ + mn_off(64 + r0, j, 2048), t);
+          for (int e = 0; e < 8; ++e) t[e] = qE[e] * pre;
+          st8_bf16(smem + OFF_WQ + mn_off(64 + r0, j, 2048), t);
+        }
         // (beta K gamma)^T, K-major [j][r]
 #pragma unroll
         for (int e = 0; e < 8; ++e) t[e] = beta_at(r0 + e) * kE[e] * pre;
@@ -459,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         sm100::tmem_wait_ld();
         if (!isk) {  // A_qk, inclusive mask; the block above the diagonal is zero
+          if (MODE == 0) {
           float t[8];
 #pragma unroll
           for (int g8 = 0; g8 < 4; ++g8) {
@@ -476,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tp.dbg_aqk[(dbo + r) * C + cb + c] = (cb + c <= r) ? v[c] : 0.0f;
             if (hf == 0)
               for (int c = 32; c < C; ++c) tp.dbg_aqk[(dbo + r) * C + c] = 0.0f;
+          }
           }
         } else {     // beta_r A_kk, strict mask, fp32 for the solve
           const float br = beta_at(r);
@@ -507,7 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((l & 31) < 16) {
           const int m = 16 * (l >> 5) + (l & 15);
           const int r = 32 + (m & 31);
-          if (m < 32) {  // A_qk[r, 0..31]
+          if (m < 32) {  // A_qk[r, 0..31] (the output needs it)
+            if (MODE == 0) {
             float t[8];
 #pragma unroll
             for (int g8 = 0; g8 < 4; ++g8) {
@@ -517,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (dbg && tp.dbg_aqk)
               for (int c = 0; c < 32; ++c) tp.dbg_aqk[(dbo + r) * C + c] = v[c];
+            }
           } else {       // beta_r A_kk[r, 0..31]
             const float br = beta_at(r);
             float4* row = reinterpret_cast<float4*>(s_akk + r * AKK_LD);
@@ -703,24 +755,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 4-7, lane = key channel); neither touches what these products read
     if (warp >= 4) {
       const int i = tid - 128;
-      float sv[64];
-#pragma unroll
-      for (int c = 0; c < 64; c += 16) {
-        float v[16];
-        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c), v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) sv[c + e] = v[e];
-      }
-      sm100::tmem_wait_ld();
-#pragma unroll
-      for (int jg = 0; jg < 8; ++jg) st8_bf16(smem + OFF_SB + mn_off(8 * jg, i, 1024), sv + 8 * jg);
       const float gc = s_gc[i];
+#pragma unroll 1
+      for (int cb = 0; cb < SC; cb += 64) {
+        float sv[64];
 #pragma unroll
-      for (int c = 0; c < 64; c += 16) {
-        uint32_t r[16];
+        for (int c = 0; c < 64; c += 16) {
+          float v[16];
+          sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + cb + c), v);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(gc * sv[c + e]);
-        sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + c), r);
+          for (int e = 0; e < 16; ++e) sv[c + e] = v[e];
+        }
+        sm100::tmem_wait_ld();
+#pragma unroll
+        for (int jg = 0; jg < 8; ++jg)
+          st8_bf16(smem + OFF_SB + mn_off(cb + 8 * jg, i, SC * 16), sv + 8 * jg);
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) {
+          uint32_t r[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(gc * sv[c + e]);
+          sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + cb + c), r);
+        }
       }
       sm100::tmem_wait_st();
     }
@@ -758,13 +814,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- (H) P = [W; Q gamma] . S -------------------------------------------
     if (tid == 0) {
-      const uint32_t idesc = sm100::idesc_bf16(128, 64, 1, 1);
+      const uint32_t idesc = sm100::idesc_bf16(128, SC, 1, 1);
       const uint32_t sa = sm100::smem_u32(smem + OFF_WQ);
       const uint32_t sb = sm100::smem_u32(smem + OFF_SB);
 #pragma unroll
       for (int s = 0; s < DK / 16; ++s)
         sm100::mma_ss(tmem + TM_P, sm100::smem_desc(sa + s * 4096, 2048, 128),
-                      sm100::smem_desc(sb + s * 2048, 1024, 128), idesc, s > 0);
+                      sm100::smem_desc(sb + s * 2 * SC * 16, SC * 16, 128), idesc, s > 0);
       commit_mma();
     }
     // the next chunk's tiles landed during this chunk: its decay factors are
@@ -798,7 +854,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e) dv[c + e] = u[e] - ws[e];
       }
 #pragma unroll
-      for (int jg = 0; jg < 8; ++jg) st8_bf16(smem + OFF_DL + mn_off(8 * jg, r, 1024), dv + 8 * jg);
+      for (int jg = 0; jg < 8; ++jg)
+        st8_bf16(smem + OFF_DL + mn_off(8 * jg, r, SC * 16), dv + 8 * jg);
+      if (MODE == 1) {  // the transition's columns: its "U" is zero
+#pragma unroll
+        for (int c = 0; c < 64; c += 16) {
+          float wp[16];
+          sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_P + 64 + c), wp);
+          sm100::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) dv[c + e] = -wp[e];
+        }
+#pragma unroll
+        for (int jg = 0; jg < 8; ++jg)
+          st8_bf16(smem + OFF_DL + mn_off(64 + 8 * jg, r, SC * 16), dv + 8 * jg);
+      }
     }
     sm100::fence_async_smem();
     sync_all();
@@ -806,25 +876,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- (J) S += (K dec)^T Delta;  O += A_qk Delta ---------------------------
     if (tid == 0) {
-      const uint32_t id_s = sm100::idesc_bf16(128, 64, 0, 1);
+      const uint32_t id_s = sm100::idesc_bf16(128, SC, 0, 1);
       const uint32_t s_kd = sm100::smem_u32(smem + OFF_KD);
-      const uint32_t s_x = sm100::smem_u32(smem + OFF_X);
       const uint32_t s_dl = sm100::smem_u32(smem + OFF_DL);
 #pragma unroll
       for (int s = 0; s < C / 16; ++s)
         sm100::mma_ss(tmem + TM_S, sm100::smem_desc(s_kd + 256 * s, 128, 1024),
-                      sm100::smem_desc(s_dl + s * 2048, 1024, 128), id_s, 1);
+                      sm100::smem_desc(s_dl + s * 2 * SC * 16, SC * 16, 128), id_s, 1);
+      if (MODE == 0) {
+        const uint32_t id_o = sm100::idesc_bf16(128, 64, 0, 1);
+        const uint32_t s_x = sm100::smem_u32(smem + OFF_X);
 #pragma unroll
-      for (int s = 0; s < C / 16; ++s)
-        sm100::mma_ss(tmem + TM_P, sm100::smem_desc(s_x + 256 * s, 128, 1024),
-                      sm100::smem_desc(s_dl + s * 2048, 1024, 128), id_s, 1);
+        for (int s = 0; s < C / 16; ++s)
+          sm100::mma_ss(tmem + TM_P, sm100::smem_desc(s_x + 256 * s, 128, 1024),
+                        sm100::smem_desc(s_dl + s * 2048, 1024, 128), id_o, 1);
+      }
       commit_mma();
     }
     wait_mma();
     KDA_PHASE(9);
 
     // ---- (K') state checkpoint (warps 4-7, lane = key channel) ------------
-    if (p.ckpt && warp >= 4 && L == C) {
+    if (MODE == 0 && p.ckpt && warp >= 4 && L == C) {
       const int64_t done = cs + L - t0;
       if (done % p.ckpt_every == 0 && done / p.ckpt_every <= p.ckpt_max) {
         const int i = tid - 128;
@@ -842,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // ---- (K) output rows (warps 2-3, lanes 64..127 = row r) ------------------
-    if (warp == 2 || warp == 3) {
+    if (MODE == 0 && (warp == 2 || warp == 3)) {
       const int r = tid - 64;
       float o[64];
 #pragma unroll
@@ -878,14 +951,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tma_pending) sm100::mbar_wait(bar_tma, tma_parity, 200000000ull);
     if (mma_inflight) sm100::mbar_wait(bar_mma, mma_phase & 1, 200000000ull);
   }
-  if (!*s_abort && p.final_state && warp < 4) {
+  // MODE 0: the sequence's final state (from its last segment); MODE 1: the
+  // segment's zero-start final state and this half's columns of its
+  // cumulative transition into the segment scratch
+  if (!*s_abort && warp < 4) {
     const int i = tid;
-    for (int c = 0; c < DVH; c += 16) {
-      float v[16];
-      sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c), v);
-      sm100::tmem_wait_ld();
+    float* dst_s = nullptr;
+    if (MODE == 0 && sg == nseg - 1 && p.final_state) dst_s = p.final_state + sbase;
+    if (MODE == 1) dst_s = p.seg_final + segbase;
+    if (dst_s) {
+      for (int c = 0; c < DVH; c += 16) {
+        float v[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c), v);
+        sm100::tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 16; ++e) p.final_state[sbase + (int64_t)i * DV + c + e] = v[e];
+        for (int e = 0; e < 16; ++e) dst_s[(int64_t)i * DV + c + e] = v[e];
+      }
+    }
+    if (MODE == 1) {
+      float* dst_p = p.seg_P + (((int64_t)n * nseg + sg) * H + h) * (int64_t)DK * DK + half * 64;
+      for (int c = 0; c < 64; c += 16) {
+        float v[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + 64 + c), v);
+        sm100::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dst_p[(int64_t)i * DK + c + e] = v[e];
+      }
     }
   }
   sm100::tc_fence_before();
@@ -921,33 +1012,33 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H, int d) {
   return r == CUDA_SUCCESS;
 }
 
+template <int MODE>
 kda_status launch_tc(const TcParams& tp, cudaStream_t stream) {
   const kda::FwdParams& p = tp.p;
   const int64_t rows = p.cu_seqlens ? (int64_t)p.T : (int64_t)p.N * p.T;
-  if (rows == 0 || p.N > 65535 || p.H > 65535) {
-    if (rows != 0) return KDA_ERR_UNSUPPORTED;
-  }
+  const int nseg = p.nseg > 1 ? p.nseg : 1;
+  if ((int64_t)p.N * nseg > 65535 || p.H > 65535) return KDA_ERR_UNSUPPORTED;
   if (rows >= (int64_t)1 << 31) return KDA_ERR_UNSUPPORTED;
   CUtensorMap mq, mk, mg, mv;
-  // an empty batch still has states to pass through; give the maps one row
-  const int64_t mrows = rows > 0 ? rows : 1;
   if (rows > 0) {
-    if (!make_map(&mq, p.q, mrows, p.H, DK) || !make_map(&mk, p.k, mrows, p.H, DK) ||
-        !make_map(&mg, p.g, mrows, p.H, DK) || !make_map(&mv, p.v, mrows, p.H, DV))
+    if (!make_map(&mq, p.q, rows, p.H, DK) || !make_map(&mk, p.k, rows, p.H, DK) ||
+        !make_map(&mg, p.g, rows, p.H, DK) || !make_map(&mv, p.v, rows, p.H, DV))
       return KDA_ERR_CUDA;
   } else {
+    // an empty batch still passes its states through; the maps are unused
     memset(&mq, 0, sizeof(mq));
     mk = mq; mg = mq; mv = mq;
   }
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(kda_tc_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(kda_tc_fused_kernel<MODE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Lay<MODE>::SMEM_BYTES) != cudaSuccess)
       return KDA_ERR_CUDA;
     attr_set = true;
   }
-  dim3 grid(2, p.H, p.N);
-  kda_tc_fused_kernel<<<grid, kThreads, SMEM_BYTES, stream>>>(mq, mk, mg, mv, tp);
+  dim3 grid(2, p.H, p.N * nseg);
+  kda_tc_fused_kernel<MODE><<<grid, kThreads, Lay<MODE>::SMEM_BYTES, stream>>>(mq, mk, mg, mv, tp);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -974,7 +1065,16 @@ kda_status kda_launch_tc(const kda::FwdParams& p, cudaStream_t stream) {
   tp.dbg_n = -1;
   tp.dbg_h = -1;
   tp.dbg_gam = tp.dbg_aqk = tp.dbg_akk = tp.dbg_t = tp.dbg_w = tp.dbg_u = nullptr;
-  return launch_tc(tp, stream);
+  return launch_tc<0>(tp, stream);
+}
+
+kda_status kda_launch_tc_summary(const kda::FwdParams& p, cudaStream_t stream) {
+  TcParams tp;
+  tp.p = p;
+  tp.dbg_n = -1;
+  tp.dbg_h = -1;
+  tp.dbg_gam = tp.dbg_aqk = tp.dbg_akk = tp.dbg_t = tp.dbg_w = tp.dbg_u = nullptr;
+  return launch_tc<1>(tp, stream);
 }
 
 extern "C" kda_status kda_debug_intra(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -991,6 +1091,7 @@ extern "C" kda_status kda_debug_intra(const uint16_t* q, const uint16_t* k, cons
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMallocAsync(&out, (size_t)rows * H * DV * 2, s) != cudaSuccess) return KDA_ERR_CUDA;
   TcParams tp;
+  tp.p = kda::FwdParams{};
   tp.p.q = q; tp.p.k = k; tp.p.v = v; tp.p.g = g_logit; tp.p.beta = beta;
   tp.p.init_state = nullptr; tp.p.out = out; tp.p.final_state = nullptr;
   tp.p.ckpt = nullptr; tp.p.ckpt_every = 0; tp.p.ckpt_max = 0;
@@ -1008,7 +1109,7 @@ extern "C" kda_status kda_debug_intra(const uint16_t* q, const uint16_t* k, cons
   }
   tp.dbg_gam = gam ? gam : g_scratch;
   tp.dbg_aqk = aqk; tp.dbg_akk = akk; tp.dbg_t = tinv; tp.dbg_w = w; tp.dbg_u = u;
-  kda_status st = launch_tc(tp, s);
+  kda_status st = launch_tc<0>(tp, s);
   if (g_scratch) cudaFreeAsync(g_scratch, s);
   cudaFreeAsync(out, s);
   return st;

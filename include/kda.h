@@ -158,6 +158,32 @@ kda_status kda_decode(const void* q, const void* k, const void* v, const void* g
                       const void* beta, float* state, void* out, int N, int T, int H, int dk,
                       int dv, kda_dtype dtype, float scale, kda_stream_t stream);
 
+/*
+ * kda_chunk_fwd_seg -- kda_chunk_fwd (bf16, dense, dk = dv = 128) with
+ * every sequence cut into `nseg` segments of ceil(T / nseg) tokens rounded
+ * up to a multiple of 64 that run in parallel: each segment's state update
+ * is affine in its entry state (S_out = P S_in + S0, P its cumulative
+ * transition, S0 its final state from a zero start); the segments'
+ * (P, S0) are computed in parallel, a short scan resolves every entry
+ * state, and the segments then run again from those states writing the
+ * output (Kimi K3 architecture, orkas.ai, "The cost is paid in the serving
+ * stack": a cumulative transition and a zero-start state per segment, then
+ * a prefix scan).  Useful when B * H is small against the SM count.
+ * workspace: device scratch of kda_seg_workspace_bytes(B, H, nseg, dk, dv)
+ * bytes (256-byte aligned), or NULL to take it from the stream-ordered
+ * allocator.  nseg = 1 is the plain forward.  kda_chunk_fwd_ex picks a
+ * segment count by itself for dense batches that would leave most SMs idle.
+ */
+kda_status kda_chunk_fwd_seg(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                             const uint16_t* g_logit, const uint16_t* beta,
+                             const float* init_state, uint16_t* out, float* final_state, int B,
+                             int T, int H, int dk, int dv, float scale, int nseg,
+                             void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                             kda_stream_t stream);
+
+/* Scratch bytes of kda_chunk_fwd_seg (0 when nseg < 2). */
+size_t kda_seg_workspace_bytes(int B, int H, int nseg, int dk, int dv);
+
 /* Device scratch bytes kda_chunk_fwd_ex needs for these sizes (0 = none).
  * N = number of sequences (B, or the cu_seqlens count when packed). */
 size_t kda_workspace_bytes(int N, int T, int H, int dk, int dv, int dtype, int chunk_size,
