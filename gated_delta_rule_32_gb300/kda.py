@@ -47,6 +47,7 @@ _SIGS = {
     "kda_chunk_fwd_seg": (_i, [_vp] * 8 + [_i] * 5 + [ctypes.c_float, _i, _vp, ctypes.c_size_t,
                                                     _vp, _vp]),
     "kda_seg_workspace_bytes": (ctypes.c_size_t, [_i] * 5),
+    "kda_chunk_fwd_seg_static": (_i, [_vp] * 8 + [_i] * 5 + [ctypes.c_float, _i, _vp, _vp]),
     "kda_decode": (_i, [_vp] * 7 + [_i] * 6 + [ctypes.c_float, _vp]),
     "kda_chunk_fwd_ckpt": (_i, [_vp] * 8 + [_i] * 5 + [_vp, _i, ctypes.c_float, _vp, _i, _i,
                                                      _vp, _vp]),
@@ -158,6 +159,14 @@ def kda_chunk_fwd_seg(q, k, v, g_logit, beta, init_state, out, final_state, B, T
                                     _p(out), _p(final_state), B, T, H, dk, dv, float(scale),
                                     nseg, _p(workspace), workspace_bytes, _p(dev_status),
                                     _stream(stream))
+
+
+def kda_chunk_fwd_seg_static(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk,
+                             dv, scale=1.0, nseg=2, dev_status=None, stream=None) -> int:
+    return load().kda_chunk_fwd_seg_static(_p(q), _p(k), _p(v), _p(g_logit), _p(beta),
+                                           _p(init_state), _p(out), _p(final_state), B, T, H,
+                                           dk, dv, float(scale), nseg, _p(dev_status),
+                                           _stream(stream))
 
 
 def kda_seg_workspace_bytes(B, H, nseg, dk=128, dv=128) -> int:

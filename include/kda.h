@@ -181,6 +181,29 @@ kda_status kda_chunk_fwd_seg(const uint16_t* q, const uint16_t* k, const uint16_
                              void* workspace, size_t workspace_bytes, int32_t* dev_status,
                              kda_stream_t stream);
 
+/*
+ * kda_chunk_fwd_seg_static -- kda_chunk_fwd_seg (nseg >= 2) that allocates
+ * nothing: for callers that may not allocate device memory at all, such as
+ * a serving engine that has reserved every byte of HBM for its own pools,
+ * or a host framework that neither hands out a workspace nor allows one to
+ * be allocated.  (This entry point has no counterpart on the pages; it is a
+ * deployment convenience.)  The segment scratch lives in a fixed 16 MiB
+ * array compiled into the library, held by every GPU that loads it until
+ * the process exits; batches needing more (B * H * nseg > 85 at dk = dv =
+ * 128) are refused with KDA_ERR_WORKSPACE before anything is queued.  The
+ * caller still provides inputs and outputs.  The first call on a device
+ * looks up the array's device address (a runtime query, no allocation);
+ * make that first call before any stream capture.  All calls share the one
+ * array and nothing in it needs to start at zero (every value read was
+ * written earlier in the same call), so calls that overlap on the GPU race:
+ * issue them on one stream, or otherwise one at a time.
+ */
+kda_status kda_chunk_fwd_seg_static(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                    const uint16_t* g_logit, const uint16_t* beta,
+                                    const float* init_state, uint16_t* out, float* final_state,
+                                    int B, int T, int H, int dk, int dv, float scale, int nseg,
+                                    int32_t* dev_status, kda_stream_t stream);
+
 /* Scratch bytes of kda_chunk_fwd_seg (0 when nseg < 2). */
 size_t kda_seg_workspace_bytes(int B, int H, int nseg, int dk, int dv);
 
