@@ -62,11 +62,12 @@ constexpr int OFF_A2 = OFF_B1 + 16384;        // [q1'; k1']       MN-major  64 x
 constexpr int OFF_B2 = OFF_A2 + 16384;        // c0'              MN-major  32 x 128   8192
 constexpr int R1_BYTES = 98304;
 //   overlay after the Gram products:
-constexpr int AKK_LD = 68;                        // fp32 row stride (floats)
-constexpr int OFF_AKK = OFF_R1;                   // [64][68] fp32   17408
-constexpr int OFF_TF = OFF_AKK + 17408;           // [64][68] fp32   17408
-constexpr int OFF_Y = OFF_TF + 17408;             // [32][36] fp32    4608
-constexpr int OFF_T = OFF_Y + 4608;               // T bf16 K-major   8192
+constexpr int AKK_LD = 72;                        // fp32 row stride (floats)
+constexpr int OFF_AKK = OFF_R1;                   // [64][72] fp32   18432
+constexpr int OFF_TF = OFF_AKK + 18432;           // [64][72] fp32   18432
+constexpr int OFF_T = OFF_TF + 18432;             // T bf16 K-major   8192
+// [32][36] fp32 products of the block merges (4608 B), dead before T is written
+constexpr int OFF_Y = OFF_T;
 
 // The rest of the map depends on the kernel mode: MODE 0 is the forward
 // (state half: 64 value columns); MODE 1 is the segment summary, which
@@ -78,9 +79,11 @@ struct Lay {
   static constexpr int SC = MODE == 0 ? 64 : 128;          // state columns in TMEM
   static constexpr int OFF_SB = OFF_T + 8192;             // [S | P] bf16, MN-major 128 x SC
   static constexpr int OFF_DL = OFF_SB + SC * 256;         // Delta bf16, MN-major 64 x SC
-  static constexpr int OFF_X = OFF_DL + SC * 128;          // rows 0..63 of [-; A_qk] (MODE 0)
-  static constexpr int OFF_AQ = OFF_X + 8192;              // A_qk masked bf16     (MODE 0)
-  static constexpr int OFF_BV = MODE == 0 ? OFF_AQ + 8192 : OFF_X;  // (beta V)^T bf16 8192
+  // rows 0..63 of the O product's A operand [-; A_qk] are never used: the
+  // descriptor starts 8 KiB before A_qk, over Delta
+  static constexpr int OFF_X = OFF_DL;                     // (MODE 0)
+  static constexpr int OFF_AQ = OFF_DL + SC * 128;         // A_qk masked bf16 (MODE 0)
+  static constexpr int OFF_BV = MODE == 0 ? OFF_AQ + 8192 : OFF_DL + SC * 128;  // (beta V)^T
   static constexpr int R1_BYTES_M = MODE == 0 ? R1_BYTES : OFF_BV + 8192 - OFF_R1;
   // R2: [W; Q gamma] MN-major, 128 M-rows x 128 K
   static constexpr int OFF_WQ = OFF_R1 + R1_BYTES_M;
@@ -164,6 +167,56 @@ __device__ __forceinline__ float alpha_of(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(x * 1.4426950408889634f));
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + t));
   return fmaxf(r, 0.006737946999085467f);
+}
+
+// Warp-level m16n8k8 product, tf32 operands, fp32 accumulation, for the
+// 16- and 32-row block merges of the triangular solve (far below the 64-row
+// minimum of tcgen05.mma; T is rounded to bf16 afterwards, so tf32's 2^-11
+// operand rounding stays below what the rest of the path keeps).
+// Fragments (g = lane / 4, t = lane % 4):
+//   a0 = A[g][t], a1 = A[g+8][t], a2 = A[g][t+4], a3 = A[g+8][t+4]
+//   b0 = B[t][g], b1 = B[t+4][g];  d0 = D[g][2t], d1 = D[g][2t+1],
+//   d2 = D[g+8][2t], d3 = D[g+8][2t+1]
+__device__ __forceinline__ uint32_t tf32_of(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// D(16x8 tile) += A[a_row0.., a_col0 + k..] * B[b_row0 + k.., b_col0..] over
+// k in [k0, k1) (multiples of 8); A, B fp32 row-major with leading dims.
+__device__ __forceinline__ void mma_tile(float (&d)[4], const float* A, int lda, int a_row0,
+                                         int a_col0, const float* B, int ldb, int b_row0,
+                                         int b_col0, int k0, int k1, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  for (int k = k0; k < k1; k += 8) {
+    uint32_t a[4], b[2];
+    const float* Ar = A + (a_row0 + g) * lda + a_col0 + k + t;
+    a[0] = tf32_of(Ar[0]);
+    a[1] = tf32_of(Ar[8 * lda]);
+    a[2] = tf32_of(Ar[4]);
+    a[3] = tf32_of(Ar[8 * lda + 4]);
+    const float* Bc = B + (b_row0 + k + t) * ldb + b_col0 + g;
+    b[0] = tf32_of(Bc[0]);
+    b[1] = tf32_of(Bc[4 * ldb]);
+    mma_tf32(d, a, b);
+  }
+}
+// store a 16x8 accumulator tile (scaled) at D[row0.., col0..]
+__device__ __forceinline__ void store_tile(const float (&d)[4], float* D, int ldd, int row0,
+                                           int col0, float sc, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  float* r0 = D + (row0 + g) * ldd + col0 + 2 * t;
+  float* r1 = r0 + 8 * ldd;
+  *reinterpret_cast<float2*>(r0) = make_float2(sc * d[0], sc * d[1]);
+  *reinterpret_cast<float2*>(r1) = make_float2(sc * d[2], sc * d[3]);
 }
 
 // ---------------------------------------------------------------------------
@@ -597,12 +650,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm100::fence_async_smem();
     sync_all();
     KDA_PHASE(3);
-    // the landing zone is free: prefetch the next chunk
-    if (ci + 1 < nchunks) {
-      if (tid == 0) issue_tma(ci + 1);
-      tma_pending = true;
-      tma_parity = (uint32_t)((ci + 1) & 1);
-    }
 
     // ---- (E) T = (I + A_kk)^{-1}, fp32 ------------------------------------
     // (1) the four 16x16 diagonal tiles, one warp each, one column per lane,
@@ -644,71 +691,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     KDA_PHASE(15);
-    {  // (2a) Y_h = A[2h+1, 2h] T[2h, 2h]: thread = (h, r, 2 columns)
-      const int hh = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
+    // (2) level 1: Y_h = A[2h+1, 2h] T[2h, 2h], T[2h+1, 2h] = -T[2h+1, 2h+1] Y_h,
+    //     h = 0, 1; warp w < 4: h = w >> 1, 8-column tile w & 1
+    if (warp < 4) {
+      const int hh = warp >> 1, nt = (warp & 1) * 8;
       const int a1 = 2 * hh + 1, a0 = 2 * hh;
-      const float* Ar = s_akk + (16 * a1 + r) * AKK_LD + 16 * a0;
-      float y0 = 0.0f, y1 = 0.0f;
-#pragma unroll
-      for (int k2 = 0; k2 < 16; ++k2) {
-        const float av = Ar[k2];
-        const float2 tv = *reinterpret_cast<const float2*>(s_tf + (16 * a0 + k2) * AKK_LD + 16 * a0 + c0);
-        y0 = fmaf(av, tv.x, y0);
-        y1 = fmaf(av, tv.y, y1);
-      }
-      *reinterpret_cast<float2*>(s_y + (hh * 16 + r) * 36 + c0) = make_float2(y0, y1);
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_tile(d, s_akk, AKK_LD, 16 * a1, 16 * a0, s_tf, AKK_LD, 16 * a0, 16 * a0 + nt, 0, 16,
+               lane);
+      store_tile(d, s_y, 36, 16 * hh, nt, 1.0f, lane);
     }
     __syncthreads();
-    {  // (2b) T[2h+1, 2h] = -T[2h+1, 2h+1] Y_h
-      const int hh = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
+    if (warp < 4) {
+      const int hh = warp >> 1, nt = (warp & 1) * 8;
       const int a1 = 2 * hh + 1, a0 = 2 * hh;
-      const float* Tr = s_tf + (16 * a1 + r) * AKK_LD + 16 * a1;
-      float y0 = 0.0f, y1 = 0.0f;
-#pragma unroll
-      for (int k2 = 0; k2 < 16; ++k2) {
-        if (k2 <= r) {
-          const float tv = Tr[k2];
-          const float2 yv = *reinterpret_cast<const float2*>(s_y + (hh * 16 + k2) * 36 + c0);
-          y0 = fmaf(tv, yv.x, y0);
-          y1 = fmaf(tv, yv.y, y1);
-        }
-      }
-      *reinterpret_cast<float2*>(s_tf + (16 * a1 + r) * AKK_LD + 16 * a0 + c0) = make_float2(-y0, -y1);
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_tile(d, s_tf, AKK_LD, 16 * a1, 16 * a1, s_y, 36, 16 * hh, nt, 0, 16, lane);
+      store_tile(d, s_tf, AKK_LD, 16 * a1, 16 * a0 + nt, -1.0f, lane);
     }
     __syncthreads();
     KDA_PHASE(16);
-    {  // (3a) Y = A[H1, H0] T[H0, H0]: thread = (row r of 32, 4 columns)
-      const int r = tid >> 3, c0 = (tid & 7) * 4;
-      const float* Ar = s_akk + (32 + r) * AKK_LD;
-      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int k2 = 0; k2 < 32; ++k2) {
-        if (k2 >= c0) {  // T[H0, H0] is lower triangular
-          const float av = Ar[k2];
-          const float4 tv = *reinterpret_cast<const float4*>(s_tf + k2 * AKK_LD + c0);
-          y.x = fmaf(av, tv.x, y.x); y.y = fmaf(av, tv.y, y.y);
-          y.z = fmaf(av, tv.z, y.z); y.w = fmaf(av, tv.w, y.w);
-        }
-      }
-      *reinterpret_cast<float4*>(s_y + r * 36 + c0) = y;
+    // (3) level 2 on the 32x32 halves; warp w: rows 16 (w >> 2), columns 8 (w & 3)
+    {
+      const int mt = (warp >> 2) * 16, nt = (warp & 3) * 8;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      // Y = A[H1, H0] T[H0, H0] (T lower triangular: k from the tile's column)
+      mma_tile(d, s_akk, AKK_LD, 32 + mt, 0, s_tf, AKK_LD, 0, nt, nt & ~7, 32, lane);
+      store_tile(d, s_y, 36, mt, nt, 1.0f, lane);
     }
     __syncthreads();
     KDA_PHASE(17);
-    {  // (3b) T[H1, H0] = -T[H1, H1] Y
-      const int r = tid >> 3, c0 = (tid & 7) * 4;
-      const float* Tr = s_tf + (32 + r) * AKK_LD + 32;
-      float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int k2 = 0; k2 < 32; ++k2) {
-        if (k2 <= r) {  // T[H1, H1] is lower triangular
-          const float tv = Tr[k2];
-          const float4 yv = *reinterpret_cast<const float4*>(s_y + k2 * 36 + c0);
-          y.x = fmaf(tv, yv.x, y.x); y.y = fmaf(tv, yv.y, y.y);
-          y.z = fmaf(tv, yv.z, y.z); y.w = fmaf(tv, yv.w, y.w);
-        }
-      }
-      *reinterpret_cast<float4*>(s_tf + (32 + r) * AKK_LD + c0) =
-          make_float4(-y.x, -y.y, -y.z, -y.w);
+    {
+      const int mt = (warp >> 2) * 16, nt = (warp & 3) * 8;
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      // T[H1, H0] = -T[H1, H1] Y (T[H1, H1] lower triangular: k up to the row tile)
+      mma_tile(d, s_tf, AKK_LD, 32 + mt, 32, s_y, 36, 0, nt, 0, mt + 16, lane);
+      store_tile(d, s_tf, AKK_LD, 32 + mt, nt, -1.0f, lane);
     }
     __syncthreads();
     KDA_PHASE(18);
@@ -749,6 +767,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                       sm100::smem_desc(s_bv + 256 * s, 128, 1024), idesc, s > 0);
       }
       commit_mma();
+    }
+    // the landing zone has been read for the last time: prefetch the next chunk
+    if (ci + 1 < nchunks) {
+      if (tid == 32) issue_tma(ci + 1);
+      tma_pending = true;
+      tma_parity = (uint32_t)((ci + 1) & 1);
     }
     // while W^T and U are formed: bf16 copy of the entry state S (B of the
     // P product) and S <- gamma_C * S ahead of the rank-64 update (warps
