@@ -220,7 +220,7 @@ __device__ __forceinline__ void store_tile(const float (&d)[4], float* D, int ld
 }
 
 // ---------------------------------------------------------------------------
-template <int MODE>
+template <int MODE, bool DBG>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_tc_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -393,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int64_t ci = 0; ci < nchunks; ++ci) {
     const int64_t cs = t0 + ci * C;
     const int L = (t1 - cs) < C ? (int)(t1 - cs) : C;
-    const bool dbg_nh = tp.dbg_gam && n == tp.dbg_n && h == tp.dbg_h;
+    // step dumps exist only in the test-hook instantiation
+    const bool dbg_nh = DBG && tp.dbg_gam && n == tp.dbg_n && h == tp.dbg_h;
     const bool dbg = dbg_nh && half == 0;
     const int64_t dbo = ci * C;  // debug row offset
 
@@ -1036,7 +1037,7 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H, int d) {
   return r == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, bool DBG>
 kda_status launch_tc(const TcParams& tp, cudaStream_t stream) {
   const kda::FwdParams& p = tp.p;
   const int64_t rows = p.cu_seqlens ? (int64_t)p.T : (int64_t)p.N * p.T;
@@ -1055,14 +1056,14 @@ kda_status launch_tc(const TcParams& tp, cudaStream_t stream) {
   }
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(kda_tc_fused_kernel<MODE>,
+    if (cudaFuncSetAttribute(kda_tc_fused_kernel<MODE, DBG>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Lay<MODE>::SMEM_BYTES) != cudaSuccess)
       return KDA_ERR_CUDA;
     attr_set = true;
   }
   dim3 grid(2, p.H, p.N * nseg);
-  kda_tc_fused_kernel<MODE><<<grid, kThreads, Lay<MODE>::SMEM_BYTES, stream>>>(mq, mk, mg, mv, tp);
+  kda_tc_fused_kernel<MODE, DBG><<<grid, kThreads, Lay<MODE>::SMEM_BYTES, stream>>>(mq, mk, mg, mv, tp);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -1089,7 +1090,7 @@ kda_status kda_launch_tc(const kda::FwdParams& p, cudaStream_t stream) {
   tp.dbg_n = -1;
   tp.dbg_h = -1;
   tp.dbg_gam = tp.dbg_aqk = tp.dbg_akk = tp.dbg_t = tp.dbg_w = tp.dbg_u = nullptr;
-  return launch_tc<0>(tp, stream);
+  return launch_tc<0, false>(tp, stream);
 }
 
 kda_status kda_launch_tc_summary(const kda::FwdParams& p, cudaStream_t stream) {
@@ -1098,7 +1099,7 @@ kda_status kda_launch_tc_summary(const kda::FwdParams& p, cudaStream_t stream) {
   tp.dbg_n = -1;
   tp.dbg_h = -1;
   tp.dbg_gam = tp.dbg_aqk = tp.dbg_akk = tp.dbg_t = tp.dbg_w = tp.dbg_u = nullptr;
-  return launch_tc<1>(tp, stream);
+  return launch_tc<1, false>(tp, stream);
 }
 
 extern "C" kda_status kda_debug_intra(const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -1133,7 +1134,7 @@ extern "C" kda_status kda_debug_intra(const uint16_t* q, const uint16_t* k, cons
   }
   tp.dbg_gam = gam ? gam : g_scratch;
   tp.dbg_aqk = aqk; tp.dbg_akk = akk; tp.dbg_t = tinv; tp.dbg_w = w; tp.dbg_u = u;
-  kda_status st = launch_tc<0>(tp, s);
+  kda_status st = launch_tc<0, true>(tp, s);
   if (g_scratch) cudaFreeAsync(g_scratch, s);
   cudaFreeAsync(out, s);
   return st;
