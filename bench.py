@@ -260,10 +260,14 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     dtype = kda.KDA_BF16 if w.dtype == torch.bfloat16 else kda.KDA_F32
 
+    # the workspace the path asks for, allocated once like a serving engine would
+    ws_bytes = kda.kda_workspace_bytes(N, T, H, dk, dv, dtype, 0, args.algo, int(w.varlen))
+    work = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes else None
+
     def step():
         rc = kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
                                   out, fs, N, T, H, dk, dv, d["cu_seqlens"], dtype, 0, 1.0,
-                                  args.algo, None, 0, None, stream)
+                                  args.algo, work, ws_bytes, None, stream)
         if rc != 0:
             raise RuntimeError("kda_chunk_fwd_ex: " + kda.status_string(rc))
 
@@ -392,7 +396,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    ap.add_argument("--algo", type=int, default=0, help="0 auto, 1 CUDA-core, 2 tensor-core")
+    ap.add_argument("--algo", type=int, default=0,
+                    help="0 auto, 1 CUDA-core, 2 tensor-core fused, 3 tensor-core two-kernel")
     ap.add_argument("--B", type=int, default=0, help="resize (profiling captures only)")
     ap.add_argument("--H", type=int, default=0, help="resize (profiling captures only)")
     ap.add_argument("--T", type=int, default=0, help="resize (profiling captures only)")

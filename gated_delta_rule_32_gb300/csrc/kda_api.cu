@@ -42,7 +42,7 @@ kda_status check_args(const void* q, const void* k, const void* v, const void* g
   if (dtype != KDA_BF16 && dtype != KDA_F32) return KDA_ERR_UNSUPPORTED;
   if (!dim_ok(dk) || !dim_ok(dv)) return KDA_ERR_UNSUPPORTED;
   if (chunk_size != 0 && chunk_size != 16 && chunk_size != 64) return KDA_ERR_UNSUPPORTED;
-  if (algo < KDA_ALGO_AUTO || algo > KDA_ALGO_TC) return KDA_ERR_INVALID_ARG;
+  if (algo < KDA_ALGO_AUTO || algo > KDA_ALGO_SPLIT) return KDA_ERR_INVALID_ARG;
   const int esz = dtype == KDA_F32 ? 4 : 2;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
       !aligned(out, 16) || !aligned(beta, esz))
@@ -91,11 +91,37 @@ bool use_tc(int dtype, int dk, int dv, int chunk_size, int algo) {
   return kda_tc_supported(dk, dv);
 }
 
+// The two-kernel form of the tensor-core path: asked for, dense batches only.
+bool use_split(int dtype, int dk, int dv, int chunk_size, int algo, int packed, int T) {
+  if (packed || T < 1 || !use_tc(dtype, dk, dv, chunk_size, algo)) return false;
+  return algo == KDA_ALGO_SPLIT;
+}
+
 }  // namespace
 
 kda_status kda_run_segmented(const kda::FwdParams& p, int nseg, void* scratch,
                              cudaStream_t stream);
 size_t kda_seg_scratch_bytes(int N, int H, int nseg, int dk, int dv);
+kda_status kda_run_split(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+size_t kda_split_workspace_bytes(int N, int T, int H);
+size_t kda_split_min_workspace_bytes(int N, int H);
+
+// A workspace smaller than the default (but at least the minimum) runs the
+// sequence in more, shorter slices.
+static kda_status run_split_ws(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+  if (workspace) {
+    if (workspace_bytes < kda_split_min_workspace_bytes(p.N, p.H)) return KDA_ERR_WORKSPACE;
+    return kda_run_split(p, workspace, workspace_bytes, stream);
+  }
+  const size_t need = kda_split_workspace_bytes(p.N, p.T, p.H);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return KDA_ERR_CUDA;
+  kda_status st = kda_run_split(p, ws, need, stream);
+  if (cudaFreeAsync(ws, stream) != cudaSuccess && st == KDA_OK) st = KDA_ERR_CUDA;
+  return st;
+}
 
 static kda_status run_segmented_ws(const kda::FwdParams& p, int nseg, void* workspace,
                                    size_t workspace_bytes, cudaStream_t stream) {
@@ -136,9 +162,10 @@ int kda_resolve_algo(int dtype, int dk, int dv, int chunk_size, int algo) {
   if (dtype != KDA_BF16 && dtype != KDA_F32) return -1;
   if (!dim_ok(dk) || !dim_ok(dv)) return -1;
   if (chunk_size != 0 && chunk_size != 16 && chunk_size != 64) return -1;
-  if (algo < KDA_ALGO_AUTO || algo > KDA_ALGO_TC) return -1;
+  if (algo < KDA_ALGO_AUTO || algo > KDA_ALGO_SPLIT) return -1;
   const bool tc = use_tc(dtype, dk, dv, chunk_size, algo);
-  if (algo == KDA_ALGO_TC && !tc) return -1;
+  if ((algo == KDA_ALGO_TC || algo == KDA_ALGO_SPLIT) && !tc) return -1;
+  if (algo == KDA_ALGO_SPLIT) return KDA_ALGO_SPLIT;
   return tc ? KDA_ALGO_TC : KDA_ALGO_SIMT;
 }
 
@@ -146,6 +173,8 @@ size_t kda_workspace_bytes(int N, int T, int H, int dk, int dv, int dtype, int c
                            int algo, int packed) {
   if (packed || N < 1 || H < 1 || T < 1) return 0;
   if (!use_tc(dtype, dk, dv, chunk_size, algo)) return 0;
+  if (use_split(dtype, dk, dv, chunk_size, algo, packed, T))
+    return kda_split_workspace_bytes(N, T, H);
   const int nseg = auto_segments(N, T, H, sm_count());
   return nseg > 1 ? kda_seg_scratch_bytes(N, H, nseg, dk, dv) : 0;
 }
@@ -193,9 +222,7 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const vo
   kda_status st = check_args(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H, dk,
                              dv, cu_seqlens, dtype, chunk_size, algo);
   if (st != KDA_OK) return st;
-  const size_t need = kda_workspace_bytes(B, T, H, dk, dv, dtype, chunk_size, algo,
-                                          cu_seqlens != nullptr);
-  if (need > 0 && workspace && workspace_bytes < need) return KDA_ERR_WORKSPACE;
+  // (each path checks the size of a workspace it is given)
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), stream) != cudaSuccess)
     return KDA_ERR_CUDA;
@@ -205,9 +232,12 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const vo
   p.cu_seqlens = cu_seqlens; p.dev_status = dev_status;
   p.N = B; p.T = T; p.H = H; p.dk = dk; p.dv = dv; p.scale = scale;
   p.ckpt = ckpt; p.ckpt_every = ckpt_every; p.ckpt_max = ckpt_max;
-  if (algo == KDA_ALGO_TC && !use_tc(dtype, dk, dv, chunk_size, algo))
+  if ((algo == KDA_ALGO_TC || algo == KDA_ALGO_SPLIT) && !use_tc(dtype, dk, dv, chunk_size, algo))
     return KDA_ERR_UNSUPPORTED;
+  if (algo == KDA_ALGO_SPLIT && cu_seqlens) return KDA_ERR_UNSUPPORTED;
   if (!use_tc(dtype, dk, dv, chunk_size, algo)) return kda_launch_simt(p, dtype, stream);
+  if (use_split(dtype, dk, dv, chunk_size, algo, cu_seqlens != nullptr, T))
+    return run_split_ws(p, workspace, workspace_bytes, stream);
   const int nseg = (cu_seqlens || ckpt) ? 1 : auto_segments(B, T, H, sm_count());
   if (nseg <= 1) return kda_launch_tc(p, stream);
   return run_segmented_ws(p, nseg, workspace, workspace_bytes, stream);

@@ -1,0 +1,882 @@
+// kda_split.cu -- the two-kernel tensor-core forward for dense batches.
+//
+// Everything of a chunk that does not depend on the state entering it (the
+// gate, the Gram matrices, T = (I + beta A_kk)^{-1}, W = T (beta K gamma),
+// U = T (beta V), Q gamma and K e^{G_C - G}) is independent across chunks;
+// only Delta = U - W S, O = (Q gamma) S + A_qk Delta and
+// S <- gamma_C S + (K dec)^T Delta chain one chunk to the next (Towards AI
+// walkthrough, "Infrastructure co-design": the chunk-to-chunk state
+// dependency is the only serial part).  So:
+//   intra kernel  one CTA per (chunk, head, sequence), every chunk at once,
+//                 two CTAs per SM; writes one record per chunk to global
+//                 memory, laid out as the state kernel's shared-memory image;
+//   state kernel  one CTA per (half of the value channels, head, sequence);
+//                 per chunk a bulk copy of the record, two tensor-core
+//                 products and two short epilogues, the state in tensor
+//                 memory throughout.
+// The record holds the operands in the precision the fused kernel feeds its
+// own state products (bf16 W, Q gamma, K dec, A_qk; fp32 U, gamma_C), so the
+// two paths round at the same points.
+//
+// A long sequence runs in slices of chunks (intra kernel over the slice,
+// then the state kernel over it), so the record buffer stays bounded; the
+// state crosses slice boundaries through global memory.
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include "kda_common.cuh"
+#include "sm100.cuh"
+#include "kda_tc_util.cuh"
+
+namespace {
+
+using namespace kda_tc;
+
+constexpr int DK = 128, DV = 128, C = 64;
+constexpr int kThreads = 256;
+constexpr int AKK_LD = 72;
+
+// ---- chunk record (bytes) ---------------------------------------------------
+constexpr int REC_KD = 0;        // (K dec)^T, K-major [key channel j][row r]  16384
+constexpr int REC_AQ = 16384;    // A_qk masked (i <= r), K-major [r][i]         8192
+constexpr int REC_WQ = 24576;    // [W; Q gamma], MN-major 128 rows x 128 K     32768
+constexpr int REC_U = 57344;     // U fp32 [value half][c / 4][r][4]            32768
+constexpr int REC_GC = 90112;    // gamma_C fp32 [128]                             512
+constexpr int REC_BYTES = 90624;
+// the part of a record one state CTA copies: KD | AQ | WQ, its U half, gamma_C
+constexpr int ST_KD = 0, ST_AQ = 16384, ST_WQ = 24576, ST_U = 57344, ST_GC = 73728;
+constexpr int STAGE_BYTES = 74240;
+
+struct SplitParams {
+  kda::FwdParams p;
+  unsigned char* rec;  // records [N][H][c_count]
+  int c_begin;         // first chunk of the slice
+  int c_count;         // chunks in the slice
+  const float* s_in;   // state entering the slice [N][H][DK][DV] (null: zero)
+  float* s_out;        // state leaving the slice (null: not kept)
+};
+
+__device__ __forceinline__ void record_error(const kda::FwdParams& p, int* s_abort,
+                                             kda_status st) {
+  *s_abort = 1;
+  if (p.dev_status) atomicExch(p.dev_status, (int32_t)st);
+}
+
+// ===========================================================================
+// intra kernel
+// ===========================================================================
+// shared memory (bytes); 102 KiB so that two CTAs share an SM
+constexpr int I_Q = 0, I_K = 16384, I_G = 32768;  // TMA landing, 2 boxes of 64 channels each
+constexpr int I_OB = 49152;                        // Gram operands for 64 key channels
+constexpr int I_A1 = I_OB;                         // [q0; k0; q1; k1] MN-major 128 x 64
+constexpr int I_B1 = I_OB + 16384;                 // [c0; c1]          MN-major  64 x 64
+constexpr int I_A2 = I_OB + 24576;                 // [q1'; k1']        MN-major  64 x 64
+constexpr int I_B2 = I_OB + 32768;                 // c0'               MN-major  32 x 64
+constexpr int I_BKG = I_OB + 36864;                // (beta K gamma)^T K-major 128 x 64
+constexpr int I_BETA = I_BKG + 16384;              // 64 raw bf16
+constexpr int I_PT = I_BETA + 128;                 // [4 tiles][128] fp32 tile products
+constexpr int I_BAR = I_PT + 2048;
+constexpr int I_MISC = I_BAR + 64;
+constexpr int I_SMEM = I_MISC + 64;
+// overlays once the earlier contents are dead
+constexpr int I_V = I_Q;                           // V landing (after the gate read Q)
+constexpr int I_BV = I_K;                          // (beta V)^T K-major [jv][r] 128 x 64
+constexpr int I_AKK = I_OB, I_TF = I_OB + 18432;   // [64][72] fp32 each (after the Grams)
+constexpr int I_T = I_G, I_Y = I_G + 8192;         // T bf16 (8192), Y fp32 [32][36]
+static_assert(I_TF + 64 * AKK_LD * 4 <= I_BKG, "solve scratch");
+static_assert(I_Y + 32 * 36 * 4 <= I_OB, "block-merge scratch");
+// the U product reads 128 rows [T; -] from I_T: they stay inside the map
+static_assert(I_T + 16384 <= I_SMEM, "U operand rows");
+static_assert(2 * (I_SMEM + 1024) <= 233472, "two CTAs per SM");
+constexpr uint32_t I_TM_COLS = 256;
+constexpr uint32_t TM_G = 0;     // Gram products: [0, 64) diagonal halves, [64, 96) cross
+constexpr uint32_t TM_W = 0;     // W^T (after the Grams are read)
+constexpr uint32_t TM_U = 64;    // U, 128 columns
+
+__global__ void __launch_bounds__(kThreads, 2)
+    kda_tc_intra_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_g,
+                        const __grid_constant__ CUtensorMap tm_v, const SplitParams sp) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const kda::FwdParams& p = sp.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.y, n = blockIdx.z, H = p.H;
+  const int64_t cs = ((int64_t)sp.c_begin + blockIdx.x) * C;  // first token of the chunk
+  const int L = (p.T - cs) < C ? (int)(p.T - cs) : C;         // valid rows
+  const int64_t row0 = (int64_t)n * p.T + cs;
+  unsigned char* rec =
+      sp.rec + (((int64_t)n * H + h) * sp.c_count + blockIdx.x) * (int64_t)REC_BYTES;
+
+  uint64_t* bar_in = reinterpret_cast<uint64_t*>(smem + I_BAR);
+  uint64_t* bar_v = bar_in + 1;
+  uint64_t* bar_mma = bar_in + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + I_MISC);
+  int* s_abort = reinterpret_cast<int*>(smem + I_MISC + 4);
+  unsigned short* s_beta_raw = reinterpret_cast<unsigned short*>(smem + I_BETA);
+  auto beta_at = [&](int r) { return __uint_as_float((uint32_t)s_beta_raw[r] << 16); };
+  float* s_pt = reinterpret_cast<float*>(smem + I_PT);
+
+  if (warp == 0) {
+    sm100::tmem_alloc(s_tmem, I_TM_COLS);
+    sm100::tmem_relinquish();
+  }
+  if (tid == 32) {
+    sm100::mbar_init(bar_in, 1);
+    sm100::mbar_init(bar_v, 1);
+    sm100::mbar_init(bar_mma, 1);
+    sm100::fence_mbar_init();
+    const int row = (int)row0;
+    sm100::mbar_arrive_expect_tx(bar_in, 49152);
+    sm100::tma_load_3d(smem + I_Q, &tm_q, bar_in, 0, h, row);
+    sm100::tma_load_3d(smem + I_Q + 8192, &tm_q, bar_in, 64, h, row);
+    sm100::tma_load_3d(smem + I_K, &tm_k, bar_in, 0, h, row);
+    sm100::tma_load_3d(smem + I_K + 8192, &tm_k, bar_in, 64, h, row);
+    sm100::tma_load_3d(smem + I_G, &tm_g, bar_in, 0, h, row);
+    sm100::tma_load_3d(smem + I_G + 8192, &tm_g, bar_in, 64, h, row);
+  }
+  if (tid < C) {
+    const unsigned short* bg = static_cast<const unsigned short*>(p.beta);
+    s_beta_raw[tid] = tid < L ? bg[(row0 + tid) * H + h] : (unsigned short)0;
+  }
+  if (tid == 0) *s_abort = 0;
+  sm100::tc_fence_before();
+  __syncthreads();
+  sm100::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t lane_q = 32u * (warp & 3);  // this warp's TMEM lane quarter
+
+  bool in_pending = true, v_pending = false, mma_pending = false;
+  uint32_t mma_phase = 0;
+  auto wait_mma = [&]() {
+    const bool ok = sm100::mbar_wait(bar_mma, mma_phase & 1);
+    if (ok) ++mma_phase;
+    else record_error(p, s_abort, KDA_ERR_TIMEOUT);
+    mma_pending = !ok;
+    sm100::tc_fence_after();
+  };
+  auto sync_all = [&]() {
+    sm100::tc_fence_before();
+    __syncthreads();
+    sm100::tc_fence_after();
+  };
+
+  do {
+    if (!sm100::mbar_wait(bar_in, 0)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
+    else in_pending = false;
+
+    // ---- gate, pass 0: decay factors of 16 rows (tile a) of key channels
+    //      jl and 64 + jl, and the tile products -------------------------------
+    const int jl = tid & 63, a = tid >> 6;
+    float al0[16], al1[16];
+    {
+      const unsigned char* g0 = smem + I_G;
+      const unsigned char* g1 = smem + I_G + 8192;
+      float p0 = 1.0f, p1 = 1.0f;
+#pragma unroll
+      for (int s = 0; s < 16; ++s) {
+        const int r = 16 * a + s;
+        const uint32_t o = sw128_off(r, jl);
+        al0[s] = r < L ? alpha_of(ld_bf16(g0, o)) : 1.0f;
+        al1[s] = r < L ? alpha_of(ld_bf16(g1, o)) : 1.0f;
+        p0 *= al0[s];
+        p1 *= al1[s];
+      }
+      s_pt[a * 128 + jl] = p0;
+      s_pt[a * 128 + 64 + jl] = p1;
+    }
+    __syncthreads();
+    if (*s_abort) break;
+
+    // ---- gate, pass hk: key channels 64 hk .. 64 hk + 63 -------------------
+    // Row/column factors of the two-level Gram scheme (reference points: end
+    // of tile 0 for the first half, end of tile 2 for the second, end of
+    // tile 1 for the cross block), each a within-tile product E (prefix,
+    // row included) or F (suffix, row excluded) times a per-tile constant:
+    //   half 0: row e^{G_r - G_15}, col e^{G_15 - G_i}, cross col e^{G_31 - G_i}
+    //   half 1: row e^{G_r - G_47}, col e^{G_47 - G_i}, cross row e^{G_r - G_31}
+    // and the record's operands Q gamma (e^{G_r}), K dec (e^{G_C - G_r}),
+    // with (beta K gamma)^T kept for the W product.
+    auto gate_pass = [&](const float (&al)[16], const int hk) {
+      const int j = 64 * hk + jl;
+      const unsigned char* sq = smem + I_Q + hk * 8192;
+      const unsigned char* sk = smem + I_K + hk * 8192;
+      const float P0 = s_pt[j], P1 = s_pt[128 + j], P2 = s_pt[256 + j], P3 = s_pt[384 + j];
+      if (a == 0) reinterpret_cast<float*>(rec + REC_GC)[j] = P0 * P1 * P2 * P3;
+      const int pr = a >> 1, tt = a & 1;
+      // tile products are >= e^-80, so their inverses stay below e^80
+      const float invPa = __fdividef(1.0f, pr == 0 ? P0 : P2);
+      const float invPb = __fdividef(1.0f, pr == 0 ? P1 : P3);
+      const float pre = a == 0 ? 1.0f : a == 1 ? P0 : a == 2 ? P0 * P1 : P0 * P1 * P2;
+      const float post = a == 0 ? P1 * P2 * P3 : a == 1 ? P2 * P3 : a == 2 ? P3 : 1.0f;
+      const float rs = tt == 0 ? invPa : 1.0f;   // diagonal-half row factor
+      const float cf = tt == 0 ? 1.0f : invPb;   // diagonal-half column factor
+      // cross-block factor: column (first half) or row (second half)
+      const float xf = pr == 0 ? (tt == 0 ? P1 : 1.0f) : (tt == 0 ? 1.0f : P2);
+      float F[16];
+      {
+        float f = 1.0f;
+#pragma unroll
+        for (int s = 15; s >= 0; --s) { F[s] = f; f *= al[s]; }
+      }
+      float e = 1.0f;
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int r0 = 16 * a + 8 * g;  // chunk row of this group of 8
+        float qE[8], kE[8], kF[8], t[8];
+#pragma unroll
+        for (int e8 = 0; e8 < 8; ++e8) {
+          const int r = r0 + e8;
+          const uint32_t o = sw128_off(r, jl);
+          const bool ok = r < L;
+          const float qv = ok ? ld_bf16(sq, o) * p.scale : 0.0f;
+          const float kv = ok ? ld_bf16(sk, o) : 0.0f;
+          e *= al[8 * g + e8];
+          qE[e8] = qv * e;
+          kE[e8] = kv * e;
+          kF[e8] = kv * F[8 * g + e8];
+        }
+        if (pr == 0) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = qE[i] * rs;
+          st8_bf16(smem + I_A1 + mn_off(r0, jl, 2048), t);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = kE[i] * rs;
+          st8_bf16(smem + I_A1 + mn_off(32 + r0, jl, 2048), t);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = kF[i] * cf;
+          st8_bf16(smem + I_B1 + mn_off(r0, jl, 1024), t);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = kF[i] * xf;
+          st8_bf16(smem + I_B2 + mn_off(r0, jl, 512), t);
+        } else {
+          const int rr0 = r0 - 32;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = qE[i] * rs;
+          st8_bf16(smem + I_A1 + mn_off(64 + rr0, jl, 2048), t);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = kE[i] * rs;
+          st8_bf16(smem + I_A1 + mn_off(96 + rr0, jl, 2048), t);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = qE[i] * xf;
+          st8_bf16(smem + I_A2 + mn_off(rr0, jl, 1024), t);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = kE[i] * xf;
+          st8_bf16(smem + I_A2 + mn_off(32 + rr0, jl, 1024), t);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = kF[i] * cf;
+          st8_bf16(smem + I_B1 + mn_off(32 + rr0, jl, 1024), t);
+        }
+        // Q gamma into rows 64.. of the record's [W; Q gamma]
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = qE[i] * pre;
+        st8_bf16(rec + REC_WQ + mn_off(64 + r0, j, 2048), t);
+        // (beta K gamma)^T, K-major [j][r]
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = beta_at(r0 + i) * kE[i] * pre;
+        st8_bf16(smem + I_BKG + k64_off(j, r0), t);
+        // (K e^{G_C - G})^T, K-major [j][r]
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = kF[i] * post;
+        st8_bf16(rec + REC_KD + k64_off(j, r0), t);
+      }
+    };
+    // Gram products over the 64 key channels of one pass: diagonal halves
+    // (M = 128, N = 64) and the cross block (M = 64, N = 32)
+    auto gram_mma = [&](const int hk) {
+      if (tid == 0) {
+        const uint32_t id1 = sm100::idesc_bf16(128, 64, 1, 1);
+        const uint32_t id2 = sm100::idesc_bf16(64, 32, 1, 1);
+        const uint32_t a1 = sm100::smem_u32(smem + I_A1), b1 = sm100::smem_u32(smem + I_B1);
+        const uint32_t a2 = sm100::smem_u32(smem + I_A2), b2 = sm100::smem_u32(smem + I_B2);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          sm100::mma_ss(tmem + TM_G, sm100::smem_desc(a1 + s * 4096, 2048, 128),
+                        sm100::smem_desc(b1 + s * 2048, 1024, 128), id1, (hk | s) > 0);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          sm100::mma_ss(tmem + TM_G + 64, sm100::smem_desc(a2 + s * 2048, 1024, 128),
+                        sm100::smem_desc(b2 + s * 1024, 512, 128), id2, (hk | s) > 0);
+        sm100::mma_commit(bar_mma);
+      }
+      mma_pending = true;
+    };
+
+    gate_pass(al0, 0);
+    sm100::fence_async_smem();
+    sync_all();
+    gram_mma(0);
+    wait_mma();
+    gate_pass(al1, 1);
+    sm100::fence_async_smem();
+    sync_all();
+    if (*s_abort) break;
+    // Q, K and G have been read for the last time: V lands over Q
+    if (tid == 32) {
+      const int row = (int)row0;
+      sm100::mbar_arrive_expect_tx(bar_v, 16384);
+      sm100::tma_load_3d(smem + I_V, &tm_v, bar_v, 0, h, row);
+      sm100::tma_load_3d(smem + I_V + 8192, &tm_v, bar_v, 64, h, row);
+    }
+    v_pending = true;
+    gram_mma(1);
+    wait_mma();
+
+    // ---- Gram epilogue (warps 0-3) | (beta V)^T (warps 4-7) -----------------
+    float* s_akk = reinterpret_cast<float*>(smem + I_AKK);
+    if (warp < 4) {
+      const int l = tid;  // TMEM lane
+      {  // diagonal halves: lane l holds row (l & 31) of q0 | k0 | q1 | k1
+        const int part = l >> 5, rl = l & 31;
+        const int hf = part >> 1, isk = part & 1;
+        const int r = 32 * hf + rl, cb = 32 * hf;
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+          float w16[16];
+          sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_G + cb + c), w16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[c + e] = w16[e];
+        }
+        sm100::tmem_wait_ld();
+        if (!isk) {  // A_qk, inclusive mask; the block right of the diagonal is zero
+          float t[8];
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t[e] = (cb + 8 * g8 + e <= r) ? v[8 * g8 + e] : 0.0f;
+            st8_bf16(rec + REC_AQ + k64_off(r, cb + 8 * g8), t);
+          }
+          if (hf == 0) {
+            const float z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) st8_bf16(rec + REC_AQ + k64_off(r, 32 + 8 * g8), z);
+          }
+        } else {     // beta_r A_kk, strict mask, fp32 for the solve
+          const float br = beta_at(r);
+          float4* row = reinterpret_cast<float4*>(s_akk + r * AKK_LD + cb);
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            float t4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = 4 * c4 + e;
+              t4[e] = (cb + c < r) ? br * v[c] : 0.0f;
+            }
+            row[c4] = make_float4(t4[0], t4[1], t4[2], t4[3]);
+          }
+        }
+      }
+      {  // cross block (rows 32..63 x columns 0..31): product row m in lane
+         // 32 (m / 16) + m % 16
+        float v[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 16) {
+          float w16[16];
+          sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_G + 64 + c), w16);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[c + e] = w16[e];
+        }
+        sm100::tmem_wait_ld();
+        if ((l & 31) < 16) {
+          const int m = 16 * (l >> 5) + (l & 15);
+          const int r = 32 + (m & 31);
+          if (m < 32) {  // A_qk[r, 0..31]
+            float t[8];
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) t[e] = v[8 * g8 + e];
+              st8_bf16(rec + REC_AQ + k64_off(r, 8 * g8), t);
+            }
+          } else {       // beta_r A_kk[r, 0..31]
+            const float br = beta_at(r);
+            float4* row = reinterpret_cast<float4*>(s_akk + r * AKK_LD);
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4)
+              row[c4] = make_float4(br * v[4 * c4], br * v[4 * c4 + 1], br * v[4 * c4 + 2],
+                                    br * v[4 * c4 + 3]);
+          }
+        }
+      }
+    } else {
+      // (beta V)^T, K-major [value channel jv][row r]
+      if (!sm100::mbar_wait(bar_v, 0)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
+      const int jv = tid - 128;
+      const unsigned char* sv = smem + I_V + (jv >> 6) * 8192;
+#pragma unroll
+      for (int g8 = 0; g8 < 8; ++g8) {
+        float t[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int r = 8 * g8 + e;
+          t[e] = (r < L) ? beta_at(r) * ld_bf16(sv, sw128_off(r, jv & 63)) : 0.0f;
+        }
+        st8_bf16(smem + I_BV + k64_off(jv, 8 * g8), t);
+      }
+    }
+    sm100::fence_async_smem();
+    sync_all();
+    if (*s_abort) break;
+    v_pending = false;
+
+    // ---- T = (I + beta A_kk)^{-1} -------------------------------------------
+    unit_lower_inverse<AKK_LD>(s_akk, reinterpret_cast<float*>(smem + I_TF),
+                               reinterpret_cast<float*>(smem + I_Y), smem + I_T, tid);
+    sm100::fence_async_smem();
+    sync_all();
+
+    // ---- W^T = (beta K gamma)^T T^T and U = [T; -] (beta V) ------------------
+    if (tid == 0) {
+      const uint32_t idw = sm100::idesc_bf16(128, 64, 0, 0);
+      const uint32_t idu = sm100::idesc_bf16(128, 128, 0, 0);
+      const uint32_t s_bkg = sm100::smem_u32(smem + I_BKG);
+      const uint32_t s_t = sm100::smem_u32(smem + I_T);
+      const uint32_t s_bv = sm100::smem_u32(smem + I_BV);
+#pragma unroll
+      for (int s = 0; s < C / 16; ++s)
+        sm100::mma_ss(tmem + TM_W, sm100::smem_desc(s_bkg + 256 * s, 128, 1024),
+                      sm100::smem_desc(s_t + 256 * s, 128, 1024), idw, s > 0);
+#pragma unroll
+      for (int s = 0; s < C / 16; ++s)
+        sm100::mma_ss(tmem + TM_U, sm100::smem_desc(s_t + 256 * s, 128, 1024),
+                      sm100::smem_desc(s_bv + 256 * s, 128, 1024), idu, s > 0);
+      sm100::mma_commit(bar_mma);
+    }
+    mma_pending = true;
+    wait_mma();
+    if (*s_abort) break;
+
+    // ---- record: W rows (all warps: lane = key channel, 32 rows each) and
+    //      U (warps 0, 1, 4, 5: lane = row, one value half each) -------------
+    {
+      const int j = tid & 127, rb = (warp >> 2) * 32;
+      float wv[32];
+#pragma unroll
+      for (int c = 0; c < 32; c += 16) {
+        float v[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_W + rb + c), v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) wv[c + e] = v[e];
+      }
+      sm100::tmem_wait_ld();
+#pragma unroll
+      for (int rg = 0; rg < 4; ++rg)
+        st8_bf16(rec + REC_WQ + mn_off(rb + 8 * rg, j, 2048), wv + 8 * rg);
+    }
+    if ((warp & 3) < 2) {
+      const int r = (warp & 1) * 32 + lane, hf = warp >> 2;
+      float4* dst = reinterpret_cast<float4*>(rec + REC_U + hf * 16384);
+#pragma unroll
+      for (int c = 0; c < 64; c += 16) {
+        float u[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_U + 64 * hf + c), u);
+        sm100::tmem_wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          dst[(c / 4 + q4) * 64 + r] =
+              make_float4(u[4 * q4], u[4 * q4 + 1], u[4 * q4 + 2], u[4 * q4 + 3]);
+      }
+    }
+  } while (0);
+
+  // after an abort: bounded waits for copies and products still in flight
+  // before the shared and tensor memory are released
+  if (*s_abort) {
+    if (in_pending) sm100::mbar_wait(bar_in, 0, 200000000ull);
+    if (v_pending) sm100::mbar_wait(bar_v, 0, 200000000ull);
+    if (mma_pending) sm100::mbar_wait(bar_mma, mma_phase & 1, 200000000ull);
+  }
+  sm100::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) sm100::tmem_dealloc(tmem, I_TM_COLS);
+}
+
+// ===========================================================================
+// state kernel
+// ===========================================================================
+constexpr int S_SB = 2 * STAGE_BYTES;  // S bf16, MN-major (K = key channel) 128 x 64
+constexpr int S_DL = S_SB + 16384;     // Delta bf16, MN-major (K = row) 64 x 64
+constexpr int S_BAR = S_DL + 8192;
+constexpr int S_MISC = S_BAR + 64;
+constexpr int S_SMEM = S_MISC + 64;
+static_assert(S_SMEM <= 232448, "shared memory");
+constexpr uint32_t S_TM_COLS = 256;
+constexpr uint32_t TM_S = 0;    // state half: 128 lanes (key channel) x 64 columns
+constexpr uint32_t TM_P = 64;   // two buffers of [W S; Q gamma S (+ A_qk Delta)], 64 columns each
+
+__global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitParams sp) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const kda::FwdParams& p = sp.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int half = blockIdx.x, h = blockIdx.y, n = blockIdx.z, H = p.H;
+  const int nc = sp.c_count;
+  const unsigned char* rec0 =
+      sp.rec + ((int64_t)n * H + h) * (int64_t)sp.c_count * REC_BYTES;
+  const int64_t sbase = ((int64_t)n * H + h) * (int64_t)DK * DV + half * 64;
+
+  uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem + S_BAR);  // [2]
+  uint64_t* bar_mma = bar_full + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S_MISC);
+  int* s_abort = reinterpret_cast<int*>(smem + S_MISC + 4);
+
+  auto issue = [&](int c) {  // record of chunk c into stage c & 1
+    unsigned char* st = smem + (c & 1) * STAGE_BYTES;
+    const unsigned char* src = rec0 + (int64_t)c * REC_BYTES;
+    uint64_t* bar = bar_full + (c & 1);
+    sm100::mbar_arrive_expect_tx(bar, STAGE_BYTES);
+    sm100::bulk_load(st + ST_KD, src + REC_KD, REC_U - REC_KD, bar);
+    sm100::bulk_load(st + ST_U, src + REC_U + half * 16384, 16384, bar);
+    sm100::bulk_load(st + ST_GC, src + REC_GC, 512, bar);
+  };
+
+  if (warp == 0) {
+    sm100::tmem_alloc(s_tmem, S_TM_COLS);
+    sm100::tmem_relinquish();
+  }
+  if (tid == 32) {
+    sm100::mbar_init(bar_full, 1);
+    sm100::mbar_init(bar_full + 1, 1);
+    sm100::mbar_init(bar_mma, 1);
+    sm100::fence_mbar_init();
+    if (nc > 0) issue(0);
+    if (nc > 1) issue(1);
+  }
+  if (tid == 0) *s_abort = 0;
+  sm100::tc_fence_before();
+  __syncthreads();
+  sm100::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t lane_q = 32u * (warp & 3);
+
+  // entry state into TMEM (lane = key channel)
+  if (warp < 4) {
+    const int i = tid;
+    for (int c = 0; c < 64; c += 16) {
+      uint32_t r[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        r[e] = __float_as_uint(sp.s_in ? sp.s_in[sbase + (int64_t)i * DV + c + e] : 0.0f);
+      sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + c), r);
+    }
+    sm100::tmem_wait_st();
+  }
+
+  uint32_t mma_phase = 0;
+  bool mma_pending = false;
+  int issued = nc < 2 ? nc : 2;  // chunks whose record copy has been issued
+  int landed = 0;                 // chunks whose record copy has been waited for
+  auto wait_mma = [&]() {
+    const bool ok = sm100::mbar_wait(bar_mma, mma_phase & 1);
+    if (ok) ++mma_phase;
+    else record_error(p, s_abort, KDA_ERR_TIMEOUT);
+    mma_pending = !ok;
+    sm100::tc_fence_after();
+  };
+  auto sync_all = [&]() {
+    sm100::tc_fence_before();
+    __syncthreads();
+    sm100::tc_fence_after();
+  };
+  // output rows of chunk c (warps 6-7: TMEM lanes 64..127 = rows 0..63)
+  auto write_out = [&](int c) {
+    const int r = tid - 192;
+    const int64_t cs = ((int64_t)sp.c_begin + c) * C;
+    const int L = (p.T - cs) < C ? (int)(p.T - cs) : C;
+    float o[64];
+#pragma unroll
+    for (int c16 = 0; c16 < 64; c16 += 16) {
+      float v[16];
+      sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_P + 64 * (c & 1) + c16), v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) o[c16 + e] = v[e];
+    }
+    sm100::tmem_wait_ld();
+    if (r < L) {
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
+                           (((int64_t)n * p.T + cs + r) * H + h) * DV + half * 64;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        const uint4 w = make_uint4(sm100::pack_bf16x2(o[8 * g], o[8 * g + 1]),
+                                   sm100::pack_bf16x2(o[8 * g + 2], o[8 * g + 3]),
+                                   sm100::pack_bf16x2(o[8 * g + 4], o[8 * g + 5]),
+                                   sm100::pack_bf16x2(o[8 * g + 6], o[8 * g + 7]));
+        *reinterpret_cast<uint4*>(dst + 8 * g) = w;
+      }
+    }
+  };
+  sync_all();
+
+  for (int c = 0; c < nc; ++c) {
+    const int s = c & 1;
+    const unsigned char* st = smem + s * STAGE_BYTES;
+    const uint32_t tm_p = TM_P + 64 * s;
+    if (!sm100::mbar_wait(bar_full + s, (uint32_t)((c >> 1) & 1)))
+      record_error(p, s_abort, KDA_ERR_TIMEOUT);
+    else
+      landed = c + 1;
+
+    // (1) bf16 copy of S (B of the P product) and S <- gamma_C S ahead of the
+    //     rank-64 update (warps 0-3, lane = key channel) | output rows of the
+    //     previous chunk (warps 6-7)
+    if (warp < 4) {
+      const int i = tid;
+      const float gc = reinterpret_cast<const float*>(st + ST_GC)[i];
+      float sv[64];
+#pragma unroll
+      for (int c16 = 0; c16 < 64; c16 += 16) {
+        float v[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c16), v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sv[c16 + e] = v[e];
+      }
+      sm100::tmem_wait_ld();
+#pragma unroll
+      for (int jg = 0; jg < 8; ++jg)
+        st8_bf16(smem + S_SB + mn_off(8 * jg, i, 1024), sv + 8 * jg);
+#pragma unroll
+      for (int c16 = 0; c16 < 64; c16 += 16) {
+        uint32_t r[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(gc * sv[c16 + e]);
+        sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + c16), r);
+      }
+      sm100::tmem_wait_st();
+    } else if (warp >= 6 && c > 0) {
+      write_out(c - 1);
+    }
+    sm100::fence_async_smem();
+    sync_all();
+    if (*s_abort) break;
+
+    // (2) P = [W; Q gamma] S
+    if (tid == 0) {
+      const uint32_t idesc = sm100::idesc_bf16(128, 64, 1, 1);
+      const uint32_t sa = sm100::smem_u32(st + ST_WQ);
+      const uint32_t sb = sm100::smem_u32(smem + S_SB);
+#pragma unroll
+      for (int k = 0; k < DK / 16; ++k)
+        sm100::mma_ss(tmem + tm_p, sm100::smem_desc(sa + k * 4096, 2048, 128),
+                      sm100::smem_desc(sb + k * 2048, 1024, 128), idesc, k > 0);
+      sm100::mma_commit(bar_mma);
+    }
+    mma_pending = true;
+    wait_mma();
+
+    // (3) Delta = U - W S (warps 0, 1, 4, 5: lane = row, 32 columns each)
+    if ((warp & 3) < 2) {
+      const int r = (warp & 1) * 32 + lane, cb = (warp >> 2) * 32;
+      float d[32];
+#pragma unroll
+      for (int c16 = 0; c16 < 32; c16 += 16) {
+        float v[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, tm_p + cb + c16), v);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) d[c16 + e] = v[e];
+      }
+      sm100::tmem_wait_ld();
+      const float4* u4 = reinterpret_cast<const float4*>(st + ST_U);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 u = u4[(cb / 4 + q) * 64 + r];
+        d[4 * q] = u.x - d[4 * q];
+        d[4 * q + 1] = u.y - d[4 * q + 1];
+        d[4 * q + 2] = u.z - d[4 * q + 2];
+        d[4 * q + 3] = u.w - d[4 * q + 3];
+      }
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        st8_bf16(smem + S_DL + mn_off(cb + 8 * g, r, 1024), d + 8 * g);
+    }
+    sm100::fence_async_smem();
+    sync_all();
+    if (*s_abort) break;
+
+    // (4) S += (K dec)^T Delta;  O = Q gamma S + A_qk Delta (rows 64.. of P;
+    //     the A operand [-; A_qk] starts 8 KiB before A_qk, inside K dec, and
+    //     its unused product rows land on the consumed W S rows)
+    if (tid == 0) {
+      const uint32_t id = sm100::idesc_bf16(128, 64, 0, 1);
+      const uint32_t s_kd = sm100::smem_u32(st + ST_KD);
+      const uint32_t s_x = sm100::smem_u32(st + ST_AQ - 8192);
+      const uint32_t s_dl = sm100::smem_u32(smem + S_DL);
+#pragma unroll
+      for (int k = 0; k < C / 16; ++k)
+        sm100::mma_ss(tmem + TM_S, sm100::smem_desc(s_kd + 256 * k, 128, 1024),
+                      sm100::smem_desc(s_dl + k * 2048, 1024, 128), id, 1);
+#pragma unroll
+      for (int k = 0; k < C / 16; ++k)
+        sm100::mma_ss(tmem + tm_p, sm100::smem_desc(s_x + 256 * k, 128, 1024),
+                      sm100::smem_desc(s_dl + k * 2048, 1024, 128), id, 1);
+      sm100::mma_commit(bar_mma);
+    }
+    mma_pending = true;
+    wait_mma();
+    if (*s_abort) break;
+    // the stage has been read for the last time: the record two chunks ahead
+    if (c + 2 < nc) {
+      if (tid == 32) issue(c + 2);
+      issued = c + 3;
+    }
+
+    // (5) state checkpoint (warps 0-3, lane = key channel)
+    if (p.ckpt && warp < 4) {
+      const int64_t cs = ((int64_t)sp.c_begin + c) * C;
+      const int L = (p.T - cs) < C ? (int)(p.T - cs) : C;
+      const int64_t done = cs + L;
+      if (L == C && done % p.ckpt_every == 0 && done / p.ckpt_every <= p.ckpt_max) {
+        const int i = tid;
+        float* dst = p.ckpt + ((((int64_t)n * H + h) * p.ckpt_max + done / p.ckpt_every - 1) *
+                                   DK + i) * DV + half * 64;
+#pragma unroll
+        for (int c16 = 0; c16 < 64; c16 += 16) {
+          float v[16];
+          sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c16), v);
+          sm100::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(dst + c16 + e) =
+                make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        }
+      }
+    }
+  }
+
+  if (*s_abort) {
+    // bounded waits for copies and products still in flight
+    if (mma_pending) sm100::mbar_wait(bar_mma, mma_phase & 1, 200000000ull);
+    for (int k = landed; k < issued; ++k)
+      sm100::mbar_wait(bar_full + (k & 1), (uint32_t)((k >> 1) & 1), 200000000ull);
+  } else {
+    if (nc > 0 && warp >= 6) write_out(nc - 1);
+    if (sp.s_out && warp < 4) {
+      const int i = tid;
+      float* dst = sp.s_out + sbase + (int64_t)i * DV;
+      for (int c16 = 0; c16 < 64; c16 += 16) {
+        float v[16];
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c16), v);
+        sm100::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<float4*>(dst + c16 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+      }
+    }
+  }
+  sm100::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) sm100::tmem_dealloc(tmem, S_TM_COLS);
+}
+
+// default bytes of records held at once (the slice length follows from it)
+constexpr size_t kRecordBudget = (size_t)4 << 30;
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t carry_bytes(int N, int H) { return align256((size_t)N * H * DK * DV * sizeof(float)); }
+
+}  // namespace
+
+// Device bytes of the two-kernel path: the state carried between slices,
+// then the records of one slice.  The default holds up to 4 GiB of records;
+// the minimum holds one chunk's records per (sequence, head).
+size_t kda_split_workspace_bytes(int N, int T, int H) {
+  if (N < 1 || H < 1 || T < 1) return 0;
+  const int64_t nchunks = ((int64_t)T + C - 1) / C;
+  const size_t per = (size_t)N * H * REC_BYTES;
+  int64_t slice = (int64_t)(kRecordBudget / per);
+  if (slice < 1) slice = 1;
+  if (slice > nchunks) slice = nchunks;
+  return carry_bytes(N, H) + per * (size_t)slice;
+}
+size_t kda_split_min_workspace_bytes(int N, int H) {
+  if (N < 1 || H < 1) return 0;
+  return carry_bytes(N, H) + (size_t)N * H * REC_BYTES;
+}
+
+namespace {
+
+// The slices run back to back on `stream`; a slice is the intra kernel over
+// its chunks, then the state kernel over the same chunks.  `stages` selects
+// the kernels (bit 0 intra, bit 1 state); `one_slice` refuses a workspace
+// that would need more than one slice.
+kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream, int stages, bool one_slice) {
+  if (p.cu_seqlens || p.dk != DK || p.dv != DV || p.T < 1) return KDA_ERR_UNSUPPORTED;
+  if (p.N > 65535 || p.H > 65535) return KDA_ERR_UNSUPPORTED;
+  const int64_t rows = (int64_t)p.N * p.T;
+  if (rows >= (int64_t)1 << 31) return KDA_ERR_UNSUPPORTED;
+  if (((uintptr_t)workspace & 255) != 0) return KDA_ERR_MISALIGNED;
+  const size_t carry = carry_bytes(p.N, p.H);
+  const size_t per = (size_t)p.N * p.H * REC_BYTES;
+  if (workspace_bytes < carry + per) return KDA_ERR_WORKSPACE;
+  const int nchunks = (int)(((int64_t)p.T + C - 1) / C);
+  const size_t fit = (workspace_bytes - carry) / per;
+  const int slice = fit < (size_t)nchunks ? (int)fit : nchunks;
+  if (one_slice && slice < nchunks) return KDA_ERR_WORKSPACE;
+  CUtensorMap mq, mk, mg, mv;
+  if (!make_map(&mq, p.q, rows, p.H, DK) || !make_map(&mk, p.k, rows, p.H, DK) ||
+      !make_map(&mg, p.g, rows, p.H, DK) || !make_map(&mv, p.v, rows, p.H, DV))
+    return KDA_ERR_CUDA;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kda_tc_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             I_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(kda_tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             S_SMEM) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    attr_set = true;
+  }
+  // the state crosses slices in final_state when there is one (each CTA
+  // reads its part before it writes it), else in the workspace
+  float* ws_carry = static_cast<float*>(workspace);
+  float* through = p.final_state ? p.final_state : ws_carry;
+  unsigned char* rec = static_cast<unsigned char*>(workspace) + carry;
+  for (int c0 = 0; c0 < nchunks; c0 += slice) {
+    const int cnt = nchunks - c0 < slice ? nchunks - c0 : slice;
+    const bool last = c0 + cnt == nchunks;
+    SplitParams sp;
+    sp.p = p;
+    sp.rec = rec;
+    sp.c_begin = c0;
+    sp.c_count = cnt;
+    sp.s_in = c0 == 0 ? p.init_state : through;
+    sp.s_out = last ? p.final_state : through;
+    if (stages & 1) {
+      kda_tc_intra_kernel<<<dim3(cnt, p.H, p.N), kThreads, I_SMEM, stream>>>(mq, mk, mg, mv,
+                                                                              sp);
+      if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    if (stages & 2) {
+      kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(sp);
+      if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    }
+  }
+  return KDA_OK;
+}
+
+}  // namespace
+
+kda_status kda_run_split(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+  return run_split(p, workspace, workspace_bytes, stream, 3, false);
+}
+
+extern "C" kda_status kda_split_stage(int stage, const uint16_t* q, const uint16_t* k,
+                                      const uint16_t* v, const uint16_t* g_logit,
+                                      const uint16_t* beta, const float* init_state,
+                                      uint16_t* out, float* final_state, int B, int T, int H,
+                                      float scale, void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_status, kda_stream_t stream) {
+  if (stage != 1 && stage != 2) return KDA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || T < 1 || !q || !k || !v || !g_logit || !beta || !out || !workspace)
+    return KDA_ERR_INVALID_ARG;
+  const uintptr_t pa = (uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)g_logit |
+                       (uintptr_t)out | (uintptr_t)init_state | (uintptr_t)final_state;
+  if ((pa & 15) != 0 || ((uintptr_t)beta & 1) != 0) return KDA_ERR_MISALIGNED;
+  kda::FwdParams p{};
+  p.q = q; p.k = k; p.v = v; p.g = g_logit; p.beta = beta;
+  p.init_state = init_state; p.out = out; p.final_state = final_state;
+  p.dev_status = dev_status;
+  p.N = B; p.T = T; p.H = H; p.dk = DK; p.dv = DV; p.scale = scale;
+  return run_split(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), stage,
+                   true);
+}

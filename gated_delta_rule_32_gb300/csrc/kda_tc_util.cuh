@@ -1,0 +1,227 @@
+// kda_tc_util.cuh -- device and host helpers shared by the tensor-core
+// kernels: shared-memory operand layouts, bf16 packing, the decay map on the
+// special-function unit, warp-level tf32 products for the triangular solve,
+// and the TMA tensor maps over [rows, H, d] bf16 tensors.
+#pragma once
+
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include "kda_common.cuh"
+#include "sm100.cuh"
+
+namespace kda_tc {
+// ---- operand layouts (core matrices of 8 x 16 B) ---------------------------
+// MN-major: element (mn, k) with `lbo` the K-group stride, M/N groups 128 B apart
+__device__ __forceinline__ uint32_t mn_off(int mn, int k, uint32_t lbo) {
+  return (uint32_t)(mn >> 3) * 128u + (uint32_t)(k >> 3) * lbo + (uint32_t)(k & 7) * 16u +
+         (uint32_t)(mn & 7) * 2u;
+}
+// K-major with K extent 64: K groups 128 B apart, M/N groups 1024 B apart
+__device__ __forceinline__ uint32_t k64_off(int mn, int k) {
+  return (uint32_t)(mn >> 3) * 1024u + (uint32_t)(k >> 3) * 128u + (uint32_t)(mn & 7) * 16u +
+         (uint32_t)(k & 7) * 2u;
+}
+// 128B-swizzled TMA row: element (row, ch) of a [rows][64] bf16 box
+__device__ __forceinline__ uint32_t sw128_off(int row, int ch) {
+  return (uint32_t)row * 128u + (uint32_t)(((ch >> 3) ^ (row & 7)) << 4) + (uint32_t)(ch & 7) * 2u;
+}
+__device__ __forceinline__ float ld_bf16(const unsigned char* base, uint32_t off) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + off));
+}
+
+__device__ __forceinline__ void st16(unsigned char* p, uint32_t a, uint32_t b, uint32_t c,
+                                     uint32_t d) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
+// pack 8 floats (v[0..7]) into a 16-byte chunk of bf16
+__device__ __forceinline__ void st8_bf16(unsigned char* p, const float* v) {
+  st16(p, sm100::pack_bf16x2(v[0], v[1]), sm100::pack_bf16x2(v[2], v[3]),
+       sm100::pack_bf16x2(v[4], v[5]), sm100::pack_bf16x2(v[6], v[7]));
+}
+
+__device__ __forceinline__ float alpha_of(float x) {
+  // exp(max(-softplus(x), -5)) = max(sigmoid(-x), e^-5) = max(1 / (1 + e^x), e^-5):
+  // one ex2 and one rcp on the special-function unit (flush-to-zero is exact
+  // here: e^x underflowing gives alpha = 1, overflowing gives the floor)
+  float t, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(x * 1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + t));
+  return fmaxf(r, 0.006737946999085467f);
+}
+
+// Warp-level m16n8k8 product, tf32 operands, fp32 accumulation, for the
+// 16- and 32-row block merges of the triangular solve (far below the 64-row
+// minimum of tcgen05.mma; T is rounded to bf16 afterwards, so tf32's 2^-11
+// operand rounding stays below what the rest of the path keeps).
+// Fragments (g = lane / 4, t = lane % 4):
+//   a0 = A[g][t], a1 = A[g+8][t], a2 = A[g][t+4], a3 = A[g+8][t+4]
+//   b0 = B[t][g], b1 = B[t+4][g];  d0 = D[g][2t], d1 = D[g][2t+1],
+//   d2 = D[g+8][2t], d3 = D[g+8][2t+1]
+__device__ __forceinline__ uint32_t tf32_of(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// D(16x8 tile) += A[a_row0.., a_col0 + k..] * B[b_row0 + k.., b_col0..] over
+// k in [k0, k1) (multiples of 8); A, B fp32 row-major with leading dims.
+__device__ __forceinline__ void mma_tile(float (&d)[4], const float* A, int lda, int a_row0,
+                                         int a_col0, const float* B, int ldb, int b_row0,
+                                         int b_col0, int k0, int k1, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  for (int k = k0; k < k1; k += 8) {
+    uint32_t a[4], b[2];
+    const float* Ar = A + (a_row0 + g) * lda + a_col0 + k + t;
+    a[0] = tf32_of(Ar[0]);
+    a[1] = tf32_of(Ar[8 * lda]);
+    a[2] = tf32_of(Ar[4]);
+    a[3] = tf32_of(Ar[8 * lda + 4]);
+    const float* Bc = B + (b_row0 + k + t) * ldb + b_col0 + g;
+    b[0] = tf32_of(Bc[0]);
+    b[1] = tf32_of(Bc[4 * ldb]);
+    mma_tf32(d, a, b);
+  }
+}
+// store a 16x8 accumulator tile (scaled) at D[row0.., col0..]
+__device__ __forceinline__ void store_tile(const float (&d)[4], float* D, int ldd, int row0,
+                                           int col0, float sc, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  float* r0 = D + (row0 + g) * ldd + col0 + 2 * t;
+  float* r1 = r0 + 8 * ldd;
+  *reinterpret_cast<float2*>(r0) = make_float2(sc * d[0], sc * d[1]);
+  *reinterpret_cast<float2*>(r1) = make_float2(sc * d[2], sc * d[3]);
+}
+
+// ---------------------------------------------------------------------------
+// T = (I + A)^{-1} for a strictly lower triangular 64 x 64 fp32 matrix A
+// (A = diag(beta) A_kk of one chunk), blocked by 16 x 16 tiles:
+// (1) the four diagonal tiles, two warps each, one column per group of four
+//     lanes, right-looking substitution in registers (critical path: 15
+//     FMAs), lane q of a group owning rows q, q+4, q+8, q+12 and the pivot
+//     arriving by shuffle;
+// (2) T[2h+1, 2h] = -T[2h+1, 2h+1] A[2h+1, 2h] T[2h, 2h] for h = 0, 1;
+// (3) T[H1, H0]  = -T[H1, H1] A[H1, H0] T[H0, H0] on the 32 x 32 halves.
+// Called by all 256 threads of the CTA (it synchronises them).  A is read
+// from `a` (row stride LD floats; blocks above the block diagonal are never
+// read), the strictly lower part of T is left in `tf` (same stride), `y`
+// ([32][36] fp32) is scratch, and T itself (unit diagonal, zero above) is
+// written as bf16 K-major [r][i] to `t_bf16`.
+template <int LD>
+__device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, float* y,
+                                                   unsigned char* t_bf16, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  {
+    const int blk = warp >> 1, c = (warp & 1) * 8 + (lane >> 2), q = lane & 3;
+    const float* A = a + (16 * blk) * LD + 16 * blk;
+    float a_reg[4][16];
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(A + (4 * k4 + q) * LD + 4 * i4);
+        a_reg[k4][4 * i4] = v4.x; a_reg[k4][4 * i4 + 1] = v4.y;
+        a_reg[k4][4 * i4 + 2] = v4.z; a_reg[k4][4 * i4 + 3] = v4.w;
+      }
+    }
+    float x[4];
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) x[k4] = (4 * k4 + q == c) ? 1.0f : 0.0f;
+    const int src0 = lane & ~3;
+#pragma unroll
+    for (int i = 0; i < 15; ++i) {
+      const float xi = __shfl_sync(0xffffffffu, x[i >> 2], src0 | (i & 3));
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        if (4 * k4 + q > i) x[k4] = fmaf(-a_reg[k4][i], xi, x[k4]);
+      }
+    }
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) tf[(16 * blk + 4 * k4 + q) * LD + 16 * blk + c] = x[k4];
+  }
+  __syncthreads();
+  // (2) Y_h = A[2h+1, 2h] T[2h, 2h], T[2h+1, 2h] = -T[2h+1, 2h+1] Y_h;
+  //     warp w < 4: h = w >> 1, 8-column tile w & 1
+  if (warp < 4) {
+    const int hh = warp >> 1, nt = (warp & 1) * 8;
+    const int a1 = 2 * hh + 1, a0 = 2 * hh;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_tile(d, a, LD, 16 * a1, 16 * a0, tf, LD, 16 * a0, 16 * a0 + nt, 0, 16, lane);
+    store_tile(d, y, 36, 16 * hh, nt, 1.0f, lane);
+  }
+  __syncthreads();
+  if (warp < 4) {
+    const int hh = warp >> 1, nt = (warp & 1) * 8;
+    const int a1 = 2 * hh + 1, a0 = 2 * hh;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_tile(d, tf, LD, 16 * a1, 16 * a1, y, 36, 16 * hh, nt, 0, 16, lane);
+    store_tile(d, tf, LD, 16 * a1, 16 * a0 + nt, -1.0f, lane);
+  }
+  __syncthreads();
+  // (3) level 2 on the 32 x 32 halves; warp w: rows 16 (w >> 2), columns 8 (w & 3)
+  {
+    const int mt = (warp >> 2) * 16, nt = (warp & 3) * 8;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    // Y = A[H1, H0] T[H0, H0] (T lower triangular: k from the tile's column)
+    mma_tile(d, a, LD, 32 + mt, 0, tf, LD, 0, nt, nt & ~7, 32, lane);
+    store_tile(d, y, 36, mt, nt, 1.0f, lane);
+  }
+  __syncthreads();
+  {
+    const int mt = (warp >> 2) * 16, nt = (warp & 3) * 8;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    // T[H1, H0] = -T[H1, H1] Y (T[H1, H1] lower triangular: k up to the row tile)
+    mma_tile(d, tf, LD, 32 + mt, 32, y, 36, 0, nt, 0, mt + 16, lane);
+    store_tile(d, tf, LD, 32 + mt, nt, -1.0f, lane);
+  }
+  __syncthreads();
+  // T as bf16, K-major [r][i], unit diagonal, zero above
+  for (int e = tid; e < 512; e += 256) {
+    const int r = e >> 3, i0 = (e & 7) * 8;
+    float t[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const int i = i0 + c;
+      t[c] = (i < r) ? tf[r * LD + i] : (i == r ? 1.0f : 0.0f);
+    }
+    st8_bf16(t_bf16 + k64_off(r, i0), t);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host: TMA tensor maps
+inline PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// 3-D map over a [rows, H, d] bf16 tensor: box = 64 channels x 1 head x 64 rows
+inline bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H, int d) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace kda_tc

@@ -29,6 +29,7 @@ KDA_F32 = 1
 KDA_ALGO_AUTO = 0
 KDA_ALGO_SIMT = 1
 KDA_ALGO_TC = 2
+KDA_ALGO_SPLIT = 3
 
 _lock = threading.Lock()
 _lib = None
@@ -55,6 +56,8 @@ _SIGS = {
                                                    ctypes.c_size_t, _vp]),
     "kda_host_staging_bytes": (ctypes.c_size_t, [_i] * 9),
     "kda_debug_umma": (_i, [_vp] * 3 + [_i] * 6 + [_vp, _vp]),
+    "kda_split_stage": (_i, [_i] + [_vp] * 8 + [_i] * 3 + [ctypes.c_float, _vp, ctypes.c_size_t,
+                                                        _vp, _vp]),
     "kda_debug_intra": (_i, [_vp] * 5 + [_i] * 5 + [_vp, _i, _i] + [_vp] * 6 + [_vp]),
 }
 
@@ -204,6 +207,15 @@ def kda_debug_intra(q, k, v, g_logit, beta, B, T, H, dk, dv, cu_seqlens, n, h, g
     return load().kda_debug_intra(_p(q), _p(k), _p(v), _p(g_logit), _p(beta), B, T, H, dk, dv,
                                   _p(cu_seqlens), n, h, _p(gam), _p(aqk), _p(akk), _p(tinv),
                                   _p(w), _p(u), _stream(stream))
+
+
+def kda_split_stage(stage, q, k, v, g_logit, beta, init_state, out, final_state, B, T, H,
+                    scale=1.0, workspace=None, workspace_bytes=0, dev_status=None,
+                    stream=None) -> int:
+    return load().kda_split_stage(stage, _p(q), _p(k), _p(v), _p(g_logit), _p(beta),
+                                  _p(init_state), _p(out), _p(final_state), B, T, H,
+                                  float(scale), _p(workspace), workspace_bytes, _p(dev_status),
+                                  _stream(stream))
 
 
 def kda_debug_umma(A, B, D, M, N, K, a_mode=0, b_mode=0, pack=0, dev_status=None,

@@ -82,7 +82,10 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
 typedef enum {
   KDA_ALGO_AUTO = 0,  /* tensor-core path where built, else CUDA-core path */
   KDA_ALGO_SIMT = 1,  /* fp32 CUDA-core chunked path (16-token chunks) */
-  KDA_ALGO_TC = 2     /* tcgen05/TMEM/TMA fused path (bf16, dk = dv = 128) */
+  KDA_ALGO_TC = 2,    /* tcgen05/TMEM/TMA fused path (bf16, dk = dv = 128) */
+  KDA_ALGO_SPLIT = 3  /* tensor-core path in two kernels (bf16, dk = dv = 128, dense
+                       * batches only): every chunk's state-independent part at once,
+                       * then the serial state pass; needs a workspace */
 } kda_algo;
 
 /* Human-readable name of a status code (static storage). */
@@ -116,6 +119,11 @@ kda_status kda_chunk_fwd_f32(const float* q, const float* k, const float* v,
  *   workspace   device scratch of at least kda_workspace_bytes() bytes, or
  *               NULL: the library then takes it from the stream-ordered
  *               allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ *               256-byte aligned.  The two-kernel path (KDA_ALGO_SPLIT)
+ *               also accepts less, down to one chunk record per (sequence,
+ *               head) plus the carried state (N * H * (90624 + 65536)
+ *               bytes, rounded up to 256): it then runs the sequence in
+ *               more, shorter slices; below that KDA_ERR_WORKSPACE.
  *   dev_status  NULL or one device int32; set to KDA_OK at the start of the
  *               work and to a device-detected error if one occurs.
  */
@@ -264,8 +272,26 @@ kda_status kda_debug_umma(const uint16_t* A, const uint16_t* B, float* D, int M,
                           int a_mode, int b_mode, int pack, int32_t* dev_status,
                           kda_stream_t stream);
 
-/* The path kda_chunk_fwd_ex would take for these arguments: KDA_ALGO_SIMT
- * or KDA_ALGO_TC, or -1 if the combination is unsupported. */
+/*
+ * Profiling hook (not part of the hot path): one of the two kernels of the
+ * KDA_ALGO_SPLIT path over a dense bf16 batch (dk = dv = 128), so that each
+ * can be timed on its own.  stage 1: the intra-chunk kernel, writes every
+ * chunk's record into `workspace`; stage 2: the state kernel, reads them,
+ * writes out and final_state.  The workspace must hold the whole sequence
+ * in one slice (kda_workspace_bytes(..., KDA_ALGO_SPLIT, 0) does), else
+ * KDA_ERR_WORKSPACE.  Stage 2 is meaningful only after stage 1 on the same
+ * inputs and workspace.  Asynchronous on `stream`.
+ */
+kda_status kda_split_stage(int stage, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           const uint16_t* g_logit, const uint16_t* beta,
+                           const float* init_state, uint16_t* out, float* final_state, int B,
+                           int T, int H, float scale, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, kda_stream_t stream);
+
+/* The path family kda_chunk_fwd_ex would take for these arguments:
+ * KDA_ALGO_SIMT, KDA_ALGO_TC (AUTO on the tensor cores: fused, segmented or
+ * two-kernel form by the sizes) or KDA_ALGO_SPLIT when asked for; -1 if the
+ * combination is unsupported. */
 int kda_resolve_algo(int dtype, int dk, int dv, int chunk_size, int algo);
 
 /* Library build identification (static string). */

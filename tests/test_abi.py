@@ -96,3 +96,25 @@ def test_package_fails_loudly_without_library(tmp_path):
             kda.load(str(tmp_path / "missing.so"))
     finally:
         kda._lib = saved
+
+
+def test_split_path_host_checks(lib):
+    # workspace sizing of the two-kernel path: carried state + one slice of
+    # 90624-byte chunk records per (sequence, head); packed batches need none
+    carry = 2 * 32 * 128 * 128 * 4
+    nb = kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=kda.KDA_ALGO_SPLIT)
+    assert nb == carry + 2 * 32 * 512 * 90624
+    assert kda.kda_workspace_bytes(2, 100, 1, 128, 128, algo=kda.KDA_ALGO_SPLIT) == \
+        2 * 128 * 128 * 4 + 2 * 2 * 90624
+    assert kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=kda.KDA_ALGO_SPLIT,
+                                   packed=1) == 0
+    assert kda.kda_resolve_algo(kda.KDA_BF16, 128, 128, 0, kda.KDA_ALGO_SPLIT) == \
+        kda.KDA_ALGO_SPLIT
+    assert kda.kda_resolve_algo(kda.KDA_BF16, 64, 128, 0, kda.KDA_ALGO_SPLIT) == -1
+    # the stage hook rejects bad arguments before anything is queued
+    st = dict(q=A, k=2 * A, v=3 * A, g_logit=4 * A, beta=5 * A, init_state=None, out=6 * A,
+              final_state=None, B=1, T=64, H=1, workspace=7 * A, workspace_bytes=1 << 30)
+    assert kda.kda_split_stage(3, **st) == kda.KDA_ERR_INVALID_ARG
+    assert kda.kda_split_stage(1, **dict(st, workspace=None)) == kda.KDA_ERR_INVALID_ARG
+    assert kda.kda_split_stage(1, **dict(st, q=A + 8)) == kda.KDA_ERR_MISALIGNED
+    assert kda.kda_split_stage(2, **dict(st, T=0)) == kda.KDA_ERR_INVALID_ARG

@@ -1,0 +1,182 @@
+"""The two-kernel tensor-core path (KDA_ALGO_SPLIT): every chunk's
+state-independent part in one parallel kernel, then the serial state pass.
+
+Parity against the fp64 oracle (max |gpu - ref| / max |ref| <= 1e-2 on the
+output and the final state, BF16 inputs), and the slicing contract: a
+workspace below the default runs the sequence in more slices, and since the
+state crosses a slice boundary in fp32 unchanged, the result is bit-identical
+to the one-slice run.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gated_delta_rule_32_gb300 as pkg
+from gated_delta_rule_32_gb300 import kda
+from kda_inputs import WORKLOADS, make_inputs, make_unit, small_workload
+
+pytestmark = pytest.mark.gpu
+
+SPLIT = kda.KDA_ALGO_SPLIT
+REC = 90624  # bytes of one chunk record
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from gated_delta_rule_32_gb300 import build
+    build.build()
+    kda.load()
+
+
+def rel(a, b):
+    den = np.abs(b).max()
+    return float(np.abs(a - b).max() / den) if den > 0 else float(np.abs(a).max())
+
+
+def min_ws(N, H):
+    carry = (N * H * 128 * 128 * 4 + 255) // 256 * 256
+    return carry + N * H * REC
+
+
+def run(x, workspace_bytes=None, final=True, inplace=False, scale=1.0, status=None):
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    B, T, H = x["B"], x["T"], x["H"]
+    out = torch.empty_like(d["v"])
+    s0 = d["init_state"]
+    if inplace:
+        fs = s0.clone() if s0 is not None else torch.zeros(B, H, 128, 128, device="cuda")
+        s0 = fs
+    else:
+        fs = torch.empty(B, H, 128, 128, device="cuda") if final else None
+    ws, nb = None, 0
+    if workspace_bytes is not None:
+        nb = workspace_bytes
+        ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    rc = kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], s0, out, fs, B, T, H,
+                              128, 128, None, kda.KDA_BF16, 0, scale, SPLIT, ws, nb, status,
+                              torch.cuda.current_stream())
+    assert rc == 0, kda.status_string(rc)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), (fs.cpu().numpy() if fs is not None else None)
+
+
+def ref(x, scale=1.0):
+    return oracle.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["init_state"], scale=scale)
+
+
+@pytest.mark.parametrize("T", [1, 15, 63, 64, 65, 130, 333, 1000])
+def test_split_matches_oracle(T):
+    w = small_workload("sp", B=2, T=T, H=2, dk=128, dv=128, s0_std=0.03, seed=500 + T)
+    x = make_inputs(w)
+    o, s = run(x)
+    o_ref, s_ref = ref(x)
+    assert rel(o, o_ref) <= 1e-2, rel(o, o_ref)
+    assert rel(s, s_ref) <= 1e-2, rel(s, s_ref)
+
+
+def test_split_no_initial_state_and_scale():
+    w = small_workload("sp0", B=1, T=450, H=3, dk=128, dv=128, s0_std=0.0, seed=9)
+    x = make_inputs(w)
+    sc = 128 ** -0.5
+    o, s = run(x, scale=sc)
+    o_ref, s_ref = ref(x, scale=sc)
+    assert rel(o, o_ref) <= 1e-2
+    assert rel(s, s_ref) <= 1e-2
+
+
+@pytest.mark.parametrize("case", ["all_floor", "alpha_one", "beta_zero", "beta_one"])
+def test_split_degenerate_gates(case):
+    w = small_workload("spd", B=1, T=200, H=2, dk=128, dv=128, s0_std=0.05, seed=31)
+    x = make_inputs(w)
+    if case == "all_floor":
+        x["g"] = torch.full_like(x["g"], 30.0)
+    elif case == "alpha_one":
+        x["g"] = torch.full_like(x["g"], -200.0)
+    elif case == "beta_zero":
+        x["beta"] = torch.zeros_like(x["beta"])
+        x["g"] = torch.full_like(x["g"], -4.0)
+    else:
+        x["beta"] = torch.ones_like(x["beta"])
+    o, s = run(x)
+    o_ref, s_ref = ref(x)
+    assert rel(o, o_ref) <= 1e-2
+    assert rel(s, s_ref) <= 1e-2
+
+
+@pytest.mark.parametrize("extra_chunks", [0, 1, 3])
+def test_slices_bit_identical(extra_chunks):
+    # 11 chunks with a ragged tail; slices of 1, 2 and 4 chunks
+    w = small_workload("sl", B=2, T=690, H=2, dk=128, dv=128, s0_std=0.05, seed=21)
+    x = make_inputs(w)
+    o1, s1 = run(x)
+    ws = min_ws(2, 2) + extra_chunks * 2 * 2 * REC
+    o2, s2 = run(x, workspace_bytes=ws)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(s1, s2)
+    # without a final state the carry lives in the workspace
+    o3, s3 = run(x, workspace_bytes=ws, final=False)
+    assert s3 is None
+    np.testing.assert_array_equal(o1, o3)
+    # state updated in place (init_state aliased with final_state)
+    o4, s4 = run(x, workspace_bytes=ws, inplace=True)
+    np.testing.assert_array_equal(o1, o4)
+    np.testing.assert_array_equal(s1, s4)
+
+
+def test_workspace_too_small_is_refused():
+    w = small_workload("wsr", B=1, T=128, H=2, dk=128, dv=128, seed=2)
+    x = make_inputs(w)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    out = torch.empty_like(d["v"])
+    nb = min_ws(1, 2) - 256
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    rc = kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], None, out, None, 1, 128,
+                              2, 128, 128, None, kda.KDA_BF16, 0, 1.0, SPLIT, ws, nb, None,
+                              torch.cuda.current_stream())
+    assert rc == kda.KDA_ERR_WORKSPACE
+    # packed batches are not taken by the two-kernel path
+    cu = torch.tensor([0, 100, 128], dtype=torch.int32, device="cuda")
+    rc = kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], None, out, None, 2, 128,
+                              2, 128, 128, cu, kda.KDA_BF16, 0, 1.0, SPLIT, None, 0, None,
+                              torch.cuda.current_stream())
+    assert rc == kda.KDA_ERR_UNSUPPORTED
+    assert kda.kda_resolve_algo(kda.KDA_BF16, 128, 128, 0, SPLIT) == SPLIT
+    assert kda.kda_resolve_algo(kda.KDA_F32, 128, 128, 0, SPLIT) == -1
+    assert kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=SPLIT) >= min_ws(2, 32)
+
+
+def test_split_deterministic_and_close_to_fused():
+    w = small_workload("spf", B=2, T=777, H=3, dk=128, dv=128, s0_std=0.02, seed=8)
+    x = make_inputs(w)
+    a = run(x)
+    b = run(x)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    of, sf = pkg.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                         algo=kda.KDA_ALGO_TC)
+    torch.cuda.synchronize()
+    assert rel(a[0], of.float().cpu().numpy()) <= 1e-2
+    assert rel(a[1], sf.cpu().numpy()) <= 1e-2
+
+
+def test_full_b2_h32_t32k_split_sampled():
+    # the benchmark's workload at full size; sampled (sequence, head) units
+    w = WORKLOADS["b2_h32_t32k"]
+    x = make_inputs(w)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    out, fs = pkg.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                          algo=SPLIT)
+    torch.cuda.synchronize()
+    o, s = out.float().cpu().numpy(), fs.cpu().numpy()
+    for (b, h) in [(0, 0), (1, 31), (0, 17)]:
+        u = make_unit(w, b, h)
+        args = [u[key].to(w.dtype)[None, :, None] for key in ("q", "k", "v", "g")]
+        bt = u["beta"].to(w.dtype)[None, :, None]
+        s0 = u["s0"][:, None] if w.s0_std > 0 else None
+        o_ref, s_ref = oracle.fwd(*args, bt, s0)
+        eo, es = rel(o[b, :, h], o_ref[0, :, 0]), rel(s[b, h], s_ref[0, 0])
+        assert eo <= 1e-2 and es <= 1e-2, (b, h, eo, es)
