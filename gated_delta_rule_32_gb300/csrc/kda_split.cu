@@ -56,6 +56,23 @@ struct SplitParams {
   float* s_out;        // state leaving the slice (null: not kept)
 };
 
+#ifdef KDA_PHASE_TIMING
+// cycles per phase, summed over the CTAs of (sequence 0, head 0) for the
+// intra kernel (marks 0..11) and over chunks of one state CTA (16..23);
+// instrumented builds only
+__device__ unsigned long long kda_split_cycles[32];
+#define SPLIT_MARK(k, cond)                                                    \
+  do {                                                                         \
+    if (cond) {                                                                \
+      const long long t_ = clock64();                                          \
+      atomicAdd(&kda_split_cycles[k], (unsigned long long)(t_ - t_mark));      \
+      t_mark = t_;                                                             \
+    }                                                                          \
+  } while (0)
+#else
+#define SPLIT_MARK(k, cond) do { } while (0)
+#endif
+
 __device__ __forceinline__ void record_error(const kda::FwdParams& p, int* s_abort,
                                              kda_status st) {
   *s_abort = 1;
@@ -102,6 +119,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   const kda::FwdParams& p = sp.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y, n = blockIdx.z, H = p.H;
+#ifdef KDA_PHASE_TIMING
+  long long t_mark = clock64();
+  const bool mk = tid == 0 && h == 0 && n == 0;
+#endif
   const int64_t cs = ((int64_t)sp.c_begin + blockIdx.x) * C;  // first token of the chunk
   const int L = (p.T - cs) < C ? (int)(p.T - cs) : C;         // valid rows
   const int64_t row0 = (int64_t)n * p.T + cs;
@@ -145,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   sm100::tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_q = 32u * (warp & 3);  // this warp's TMEM lane quarter
+  SPLIT_MARK(0, mk);
 
   bool in_pending = true, v_pending = false, mma_pending = false;
   uint32_t mma_phase = 0;
@@ -164,6 +186,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   do {
     if (!sm100::mbar_wait(bar_in, 0)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
     else in_pending = false;
+    SPLIT_MARK(1, mk);
 
     // ---- gate, pass 0: decay factors of 16 rows (tile a) of key channels
     //      jl and 64 + jl, and the tile products -------------------------------
@@ -186,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       s_pt[a * 128 + 64 + jl] = p1;
     }
     __syncthreads();
+    SPLIT_MARK(2, mk);
     if (*s_abort) break;
 
     // ---- gate, pass hk: key channels 64 hk .. 64 hk + 63 -------------------
@@ -305,11 +329,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     gate_pass(al0, 0);
     sm100::fence_async_smem();
     sync_all();
+    SPLIT_MARK(3, mk);
     gram_mma(0);
     wait_mma();
+    SPLIT_MARK(4, mk);
     gate_pass(al1, 1);
     sm100::fence_async_smem();
     sync_all();
+    SPLIT_MARK(5, mk);
     if (*s_abort) break;
     // Q, K and G have been read for the last time: V lands over Q
     if (tid == 32) {
@@ -321,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     v_pending = true;
     gram_mma(1);
     wait_mma();
+    SPLIT_MARK(6, mk);
 
     // ---- Gram epilogue (warps 0-3) | (beta V)^T (warps 4-7) -----------------
     float* s_akk = reinterpret_cast<float*>(smem + I_AKK);
@@ -417,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     sm100::fence_async_smem();
     sync_all();
+    SPLIT_MARK(7, mk);
     if (*s_abort) break;
     v_pending = false;
 
@@ -425,6 +454,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                                reinterpret_cast<float*>(smem + I_Y), smem + I_T, tid);
     sm100::fence_async_smem();
     sync_all();
+    SPLIT_MARK(8, mk);
 
     // ---- W^T = (beta K gamma)^T T^T and U = [T; -] (beta V) ------------------
     if (tid == 0) {
@@ -445,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     mma_pending = true;
     wait_mma();
+    SPLIT_MARK(9, mk);
     if (*s_abort) break;
 
     // ---- record: W rows (all warps: lane = key channel, 32 rows each) and
@@ -479,6 +510,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   } while (0);
+  SPLIT_MARK(10, mk);
 
   // after an abort: bounded waits for copies and products still in flight
   // before the shared and tensor memory are released
@@ -490,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   sm100::tc_fence_before();
   __syncthreads();
   if (warp == 0) sm100::tmem_dealloc(tmem, I_TM_COLS);
+  SPLIT_MARK(11, mk);
 }
 
 // ===========================================================================
@@ -511,6 +544,10 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int half = blockIdx.x, h = blockIdx.y, n = blockIdx.z, H = p.H;
   const int nc = sp.c_count;
+#ifdef KDA_PHASE_TIMING
+  long long t_mark = clock64();
+  const bool mk = tid == 0 && half == 0 && h == 0 && n == 0;
+#endif
   const unsigned char* rec0 =
       sp.rec + ((int64_t)n * H + h) * (int64_t)sp.c_count * REC_BYTES;
   const int64_t sbase = ((int64_t)n * H + h) * (int64_t)DK * DV + half * 64;
@@ -606,6 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
     }
   };
   sync_all();
+  SPLIT_MARK(16, mk);
 
   for (int c = 0; c < nc; ++c) {
     const int s = c & 1;
@@ -615,6 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
       record_error(p, s_abort, KDA_ERR_TIMEOUT);
     else
       landed = c + 1;
+    SPLIT_MARK(17, mk);
 
     // (1) bf16 copy of S (B of the P product) and S <- gamma_C S ahead of the
     //     rank-64 update (warps 0-3, lane = key channel) | output rows of the
@@ -647,6 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
     }
     sm100::fence_async_smem();
     sync_all();
+    SPLIT_MARK(18, mk);
     if (*s_abort) break;
 
     // (2) P = [W; Q gamma] S
@@ -662,6 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
     }
     mma_pending = true;
     wait_mma();
+    SPLIT_MARK(19, mk);
 
     // (3) Delta = U - W S (warps 0, 1, 4, 5: lane = row, 32 columns each)
     if ((warp & 3) < 2) {
@@ -690,6 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
     }
     sm100::fence_async_smem();
     sync_all();
+    SPLIT_MARK(20, mk);
     if (*s_abort) break;
 
     // (4) S += (K dec)^T Delta;  O = Q gamma S + A_qk Delta (rows 64.. of P;
@@ -712,6 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
     }
     mma_pending = true;
     wait_mma();
+    SPLIT_MARK(21, mk);
     if (*s_abort) break;
     // the stage has been read for the last time: the record two chunks ahead
     if (c + 2 < nc) {
@@ -740,6 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
         }
       }
     }
+    SPLIT_MARK(22, mk);
   }
 
   if (*s_abort) {
@@ -774,6 +818,19 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t carry_bytes(int N, int H) { return align256((size_t)N * H * DK * DV * sizeof(float)); }
 
 }  // namespace
+
+#ifdef KDA_PHASE_TIMING
+extern "C" int kda_split_timing_read(unsigned long long* out32, int reset) {
+  if (cudaMemcpyFromSymbol(out32, kda_split_cycles, sizeof(unsigned long long) * 32) !=
+      cudaSuccess)
+    return -1;
+  if (reset) {
+    unsigned long long z[32] = {0};
+    cudaMemcpyToSymbol(kda_split_cycles, z, sizeof(z));
+  }
+  return 0;
+}
+#endif
 
 // Device bytes of the two-kernel path: the state carried between slices,
 // then the records of one slice.  The default holds up to 4 GiB of records;
