@@ -308,6 +308,34 @@ def run_ours(args):
     tokens = w.B * w.T
     value = ws * tokens / (ms_per_step / 1e3)
 
+    # ---- the two kernels of the split path, each timed alone ----------------
+    split = (dtype == kda.KDA_BF16 and dk == 128 and dv == 128 and not w.varlen and T > 0 and
+             args.algo in (kda.KDA_ALGO_AUTO, kda.KDA_ALGO_SPLIT))
+    launches_per_step = 1
+    split_ms = {}
+    if split:
+        rec = 90624  # bytes of one chunk record
+        carry = (N * H * dk * dv * 4 + 255) // 256 * 256
+        slice_chunks = (ws_bytes - carry) // (N * H * rec)
+        nchunks = (T + 63) // 64
+        launches_per_step = 2 * ((nchunks + slice_chunks - 1) // slice_chunks)
+
+        def stage(sg):
+            return kda.kda_split_stage(sg, d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                       d["init_state"], out, fs, N, T, H, 1.0, work, ws_bytes,
+                                       None, stream)
+        if launches_per_step == 2 and stage(1) == 0 and stage(2) == 0:
+            n_k = max(3, args.steps)
+            for sg, name in ((1, "kda_tc_intra_kernel"), (2, "kda_tc_state_kernel")):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(n_k):
+                    stage(sg)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                split_ms[name] = e0.elapsed_time(e1) / n_k
+
     # ---- end to end: host buffers through kda_chunk_fwd_host ---------------
     e2e = None
     if not args.no_e2e:
@@ -351,11 +379,24 @@ def run_ours(args):
     hbm_gbs, bf16_tf, peak_src = measured_peaks()
     path = kda.kda_resolve_algo(dtype, dk, dv, 0, args.algo)
     kname = "kda_tc_fused_kernel" if path == kda.KDA_ALGO_TC else "kda_simt_kernel"
+    traffic = None
+    kernels = None
+    if split:
+        # the path is two kernels; the roofline is taken over the pair (one
+        # forward), each kernel's own time and traffic listed beside it
+        kname = "kda_tc_intra_kernel + kda_tc_state_kernel"
+        tr = [ncu_traffic(k, w.name) for k in ("kda_tc_intra_kernel", "kda_tc_state_kernel")]
+        traffic = sum(tr) if all(t is not None for t in tr) else None
+        tot = sum(split_ms.values()) if split_ms else None
+        kernels = {k: {"ms": v, "share": v / tot, "dram_bytes": ncu_traffic(k, w.name)}
+                   for k, v in split_ms.items()} if split_ms else None
+    else:
+        traffic = ncu_traffic(kname, w.name)
     kernel_ms = float(np.mean(launch_ms))
     nbytes = alg_bytes(w, x["init_state"] is not None, True)
     achieved = nbytes / (kernel_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s",
-                "frac": achieved / hbm_gbs, "traffic": ncu_traffic(kname, w.name),
+                "frac": achieved / hbm_gbs, "traffic": traffic, "kernels": kernels,
                 "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs, STREAM copy)",
                 "kernel": kname, "alg_bytes_per_launch": nbytes,
                 "kernel_ms_mean": kernel_ms,
@@ -380,7 +421,7 @@ def run_ours(args):
                        "init_state": x["init_state"] is not None,
                        "l2": "inputs %.2f GB > 129 MB L2 (no flush needed)"
                              % (nbytes / 1e9) if nbytes > 129e6 else "L2-resident"},
-            "clocks": clk, "e2e": e2e, "gpu_launches": args.steps * 1,
+            "clocks": clk, "e2e": e2e, "gpu_launches": args.steps * launches_per_step,
             "roofline": roofline, "cpu_baseline": cpu}
     print(json.dumps(line))
     if ws > 1:

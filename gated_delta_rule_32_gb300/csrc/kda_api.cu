@@ -91,10 +91,13 @@ bool use_tc(int dtype, int dk, int dv, int chunk_size, int algo) {
   return kda_tc_supported(dk, dv);
 }
 
-// The two-kernel form of the tensor-core path: asked for, dense batches only.
+// The two-kernel form of the tensor-core path: dense batches, when asked for
+// or by default (it runs every chunk's state-independent work at once; the
+// fused kernel, which repeats it per value half and runs it serially per
+// chain, stays the path of packed batches and of KDA_ALGO_TC).
 bool use_split(int dtype, int dk, int dv, int chunk_size, int algo, int packed, int T) {
   if (packed || T < 1 || !use_tc(dtype, dk, dv, chunk_size, algo)) return false;
-  return algo == KDA_ALGO_SPLIT;
+  return algo == KDA_ALGO_SPLIT || algo == KDA_ALGO_AUTO;
 }
 
 }  // namespace
@@ -302,6 +305,9 @@ size_t kda_host_staging_bytes(int B, int T, int H, int dk, int dv, int dtype, in
   if (has_init) tot += round_up(s.state);
   if (has_final) tot += round_up(s.state);
   tot += round_up(s.cu) + 256;  // cu_seqlens + device status word
+  // the path's own workspace (chunk records of the two-kernel form, or the
+  // segment scratch), so that the end-to-end call allocates nothing itself
+  tot += round_up(kda_workspace_bytes(B, T, H, dk, dv, dtype, 0, KDA_ALGO_AUTO, packed));
   return tot;
 }
 
@@ -341,6 +347,8 @@ kda_status kda_chunk_fwd_host(const void* q, const void* k, const void* v, const
   float* ds1 = final_state ? (float*)take(s.state) : nullptr;
   int32_t* dcu = packed ? (int32_t*)take(s.cu) : nullptr;
   int32_t* dstat = (int32_t*)take(sizeof(int32_t));
+  const size_t ws_bytes = kda_workspace_bytes(B, T, H, dk, dv, dtype, 0, KDA_ALGO_AUTO, packed);
+  void* ws = ws_bytes ? take(ws_bytes) : nullptr;
   kda_status st = KDA_OK;
   int32_t hstat = 0;
   bool ok = true;
@@ -358,7 +366,7 @@ kda_status kda_chunk_fwd_host(const void* q, const void* k, const void* v, const
   if (!ok) st = KDA_ERR_CUDA;
   if (st == KDA_OK)
     st = kda_chunk_fwd_ex(dq, dk_, dv_, dg, db, ds0, dout, ds1, B, T, H, dk, dv, dcu, dtype, 0,
-                          scale, KDA_ALGO_AUTO, nullptr, 0, dstat, stream_);
+                          scale, KDA_ALGO_AUTO, ws, ws_bytes, dstat, stream_);
   if (st == KDA_OK) {
     ok = cudaMemcpyAsync(out, dout, s.v, cudaMemcpyDeviceToHost, stream) == cudaSuccess;
     if (ds1)

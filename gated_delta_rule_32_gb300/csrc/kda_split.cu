@@ -95,15 +95,17 @@ constexpr int I_PT = I_BETA + 128;                 // [4 tiles][128] fp32 tile p
 constexpr int I_BAR = I_PT + 2048;
 constexpr int I_MISC = I_BAR + 64;
 constexpr int I_SMEM = I_MISC + 64;
-// overlays once the earlier contents are dead
-constexpr int I_V = I_Q;                           // V landing (after the gate read Q)
-constexpr int I_BV = I_K;                          // (beta V)^T K-major [jv][r] 128 x 64
+// V lands with Q, K, G in the Gram operand buffer, which is free until the
+// first gate pass; the rest overlays what is dead by then
+constexpr int I_V = I_OB;                          // V landing, 2 boxes (until (beta V)^T)
+constexpr int I_BV = I_G;                          // (beta V)^T K-major [jv][r] 128 x 64
 constexpr int I_AKK = I_OB, I_TF = I_OB + 18432;   // [64][72] fp32 each (after the Grams)
-constexpr int I_T = I_G, I_Y = I_G + 8192;         // T bf16 (8192), Y fp32 [32][36]
+constexpr int I_T = I_Q, I_Y = I_Q + 8192;         // T bf16 (8192), Y fp32 [32][36]
+static_assert(I_V + 16384 <= I_BKG, "V landing");
 static_assert(I_TF + 64 * AKK_LD * 4 <= I_BKG, "solve scratch");
-static_assert(I_Y + 32 * 36 * 4 <= I_OB, "block-merge scratch");
-// the U product reads 128 rows [T; -] from I_T: they stay inside the map
-static_assert(I_T + 16384 <= I_SMEM, "U operand rows");
+static_assert(I_Y + 32 * 36 * 4 <= I_K, "block-merge scratch");
+// the U product reads 128 rows [T; -] from I_T: they stay inside the Q region
+static_assert(I_T + 16384 <= I_K, "U operand rows");
 static_assert(2 * (I_SMEM + 1024) <= 233472, "two CTAs per SM");
 constexpr uint32_t I_TM_COLS = 256;
 constexpr uint32_t TM_G = 0;     // Gram products: [0, 64) diagonal halves, [64, 96) cross
@@ -118,20 +120,36 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ __align__(1024) unsigned char smem[];
   const kda::FwdParams& p = sp.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y, n = blockIdx.z, H = p.H;
+  const int H = p.H;
+  // work items: w = (n * H + h) * c_count + chunk of the slice; this CTA
+  // takes blockIdx.x, blockIdx.x + gridDim.x, ...
+  const int64_t n_items = (int64_t)p.N * H * sp.c_count;
+  struct Item {
+    int h;
+    int L;           // valid rows of the chunk
+    int64_t row0;    // global row of its first token
+    int64_t w;
+  };
+  auto item_of = [&](int64_t w) {
+    Item it;
+    const int64_t nh = w / sp.c_count, cl = w % sp.c_count;
+    it.h = (int)(nh % H);
+    const int64_t n = nh / H;
+    const int64_t cs = ((int64_t)sp.c_begin + cl) * C;
+    it.L = (p.T - cs) < C ? (int)(p.T - cs) : C;
+    it.row0 = n * p.T + cs;
+    it.w = w;
+    return it;
+  };
 #ifdef KDA_PHASE_TIMING
   long long t_mark = clock64();
-  const bool mk = tid == 0 && h == 0 && n == 0;
+  const bool mk = tid == 0 && blockIdx.x == 0;
 #endif
-  const int64_t cs = ((int64_t)sp.c_begin + blockIdx.x) * C;  // first token of the chunk
-  const int L = (p.T - cs) < C ? (int)(p.T - cs) : C;         // valid rows
-  const int64_t row0 = (int64_t)n * p.T + cs;
-  unsigned char* rec =
-      sp.rec + (((int64_t)n * H + h) * sp.c_count + blockIdx.x) * (int64_t)REC_BYTES;
 
-  uint64_t* bar_in = reinterpret_cast<uint64_t*>(smem + I_BAR);
-  uint64_t* bar_v = bar_in + 1;
-  uint64_t* bar_mma = bar_in + 2;
+  uint64_t* bar_qg = reinterpret_cast<uint64_t*>(smem + I_BAR);  // Q and G tiles
+  uint64_t* bar_k = bar_qg + 1;                                   // K tiles
+  uint64_t* bar_v = bar_qg + 2;                                   // V tiles
+  uint64_t* bar_mma = bar_qg + 3;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + I_MISC);
   int* s_abort = reinterpret_cast<int*>(smem + I_MISC + 4);
   unsigned short* s_beta_raw = reinterpret_cast<unsigned short*>(smem + I_BETA);
@@ -142,24 +160,46 @@ __global__ void __launch_bounds__(kThreads, 2)
     sm100::tmem_alloc(s_tmem, I_TM_COLS);
     sm100::tmem_relinquish();
   }
+  // the tiles of an item land region by region as the previous item's use
+  // of that region ends (issued by thread 32)
+  auto load_qg = [&](const Item& it) {
+    const int row = (int)it.row0;
+    sm100::mbar_arrive_expect_tx(bar_qg, 32768);
+    sm100::tma_load_3d(smem + I_Q, &tm_q, bar_qg, 0, it.h, row);
+    sm100::tma_load_3d(smem + I_Q + 8192, &tm_q, bar_qg, 64, it.h, row);
+    sm100::tma_load_3d(smem + I_G, &tm_g, bar_qg, 0, it.h, row);
+    sm100::tma_load_3d(smem + I_G + 8192, &tm_g, bar_qg, 64, it.h, row);
+  };
+  auto load_k = [&](const Item& it) {
+    sm100::mbar_arrive_expect_tx(bar_k, 16384);
+    sm100::tma_load_3d(smem + I_K, &tm_k, bar_k, 0, it.h, (int)it.row0);
+    sm100::tma_load_3d(smem + I_K + 8192, &tm_k, bar_k, 64, it.h, (int)it.row0);
+  };
+  auto load_v = [&](const Item& it) {
+    sm100::mbar_arrive_expect_tx(bar_v, 16384);
+    sm100::tma_load_3d(smem + I_V, &tm_v, bar_v, 0, it.h, (int)it.row0);
+    sm100::tma_load_3d(smem + I_V + 8192, &tm_v, bar_v, 64, it.h, (int)it.row0);
+  };
+  // beta of an item, kept as raw bf16 bits in a register until its slot is free
+  auto load_beta = [&](const Item& it) -> unsigned short {
+    if (tid < C && tid < it.L)
+      return static_cast<const unsigned short*>(p.beta)[(it.row0 + tid) * H + it.h];
+    return 0;
+  };
+  Item cur = item_of(blockIdx.x);
   if (tid == 32) {
-    sm100::mbar_init(bar_in, 1);
+    sm100::mbar_init(bar_qg, 1);
+    sm100::mbar_init(bar_k, 1);
     sm100::mbar_init(bar_v, 1);
     sm100::mbar_init(bar_mma, 1);
     sm100::fence_mbar_init();
-    const int row = (int)row0;
-    sm100::mbar_arrive_expect_tx(bar_in, 49152);
-    sm100::tma_load_3d(smem + I_Q, &tm_q, bar_in, 0, h, row);
-    sm100::tma_load_3d(smem + I_Q + 8192, &tm_q, bar_in, 64, h, row);
-    sm100::tma_load_3d(smem + I_K, &tm_k, bar_in, 0, h, row);
-    sm100::tma_load_3d(smem + I_K + 8192, &tm_k, bar_in, 64, h, row);
-    sm100::tma_load_3d(smem + I_G, &tm_g, bar_in, 0, h, row);
-    sm100::tma_load_3d(smem + I_G + 8192, &tm_g, bar_in, 64, h, row);
+    if (cur.w < n_items) {
+      load_qg(cur);
+      load_k(cur);
+      load_v(cur);
+    }
   }
-  if (tid < C) {
-    const unsigned short* bg = static_cast<const unsigned short*>(p.beta);
-    s_beta_raw[tid] = tid < L ? bg[(row0 + tid) * H + h] : (unsigned short)0;
-  }
+  unsigned short beta_raw = cur.w < n_items ? load_beta(cur) : (unsigned short)0;
   if (tid == 0) *s_abort = 0;
   sm100::tc_fence_before();
   __syncthreads();
@@ -168,8 +208,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t lane_q = 32u * (warp & 3);  // this warp's TMEM lane quarter
   SPLIT_MARK(0, mk);
 
-  bool in_pending = true, v_pending = false, mma_pending = false;
+  bool mma_pending = false;
   uint32_t mma_phase = 0;
+  // items whose copies were issued / waited for, per barrier
+  const int first = cur.w < n_items ? 1 : 0;
+  int qg_issued = first, k_issued = first, v_issued = first;
+  int qg_done = 0, k_done = 0, v_done = 0;
   auto wait_mma = [&]() {
     const bool ok = sm100::mbar_wait(bar_mma, mma_phase & 1);
     if (ok) ++mma_phase;
@@ -183,9 +227,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     sm100::tc_fence_after();
   };
 
-  do {
-    if (!sm100::mbar_wait(bar_in, 0)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
-    else in_pending = false;
+  for (int li = 0; cur.w < n_items; ++li) {
+    const int L = cur.L;
+    unsigned char* rec = sp.rec + cur.w * (int64_t)REC_BYTES;
+    const Item nxt = item_of(cur.w + gridDim.x);
+    const bool has_next = nxt.w < n_items;
+    const uint32_t par = (uint32_t)(li & 1);
+    if (!sm100::mbar_wait(bar_qg, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
+    else qg_done = li + 1;
+    if (tid < C) s_beta_raw[tid] = beta_raw;  // bf16 bits; readers widen them
     SPLIT_MARK(1, mk);
 
     // ---- gate, pass 0: decay factors of 16 rows (tile a) of key channels
@@ -209,8 +259,27 @@ __global__ void __launch_bounds__(kThreads, 2)
       s_pt[a * 128 + 64 + jl] = p1;
     }
     __syncthreads();
-    SPLIT_MARK(2, mk);
     if (*s_abort) break;
+    // (beta V)^T, K-major [value channel jv][row r], over the dead G tiles;
+    // V is read before the gate passes overwrite it
+    if (!sm100::mbar_wait(bar_v, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
+    else v_done = li + 1;
+    {
+      const int jv = tid & 127, rh = tid >> 7;
+      const unsigned char* sv = smem + I_V + (jv >> 6) * 8192;
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
+        float t[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int r = 32 * rh + 8 * g8 + e;
+          t[e] = (r < L) ? beta_at(r) * ld_bf16(sv, sw128_off(r, jv & 63)) : 0.0f;
+        }
+        st8_bf16(smem + I_BV + k64_off(jv, 32 * rh + 8 * g8), t);
+      }
+    }
+    __syncthreads();
+    SPLIT_MARK(2, mk);
 
     // ---- gate, pass hk: key channels 64 hk .. 64 hk + 63 -------------------
     // Row/column factors of the two-level Gram scheme (reference points: end
@@ -326,6 +395,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       mma_pending = true;
     };
 
+    if (!sm100::mbar_wait(bar_k, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
+    else k_done = li + 1;
     gate_pass(al0, 0);
     sm100::fence_async_smem();
     sync_all();
@@ -338,22 +409,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     sync_all();
     SPLIT_MARK(5, mk);
     if (*s_abort) break;
-    // Q, K and G have been read for the last time: V lands over Q
-    if (tid == 32) {
-      const int row = (int)row0;
-      sm100::mbar_arrive_expect_tx(bar_v, 16384);
-      sm100::tma_load_3d(smem + I_V, &tm_v, bar_v, 0, h, row);
-      sm100::tma_load_3d(smem + I_V + 8192, &tm_v, bar_v, 64, h, row);
+    // K has been read for the last time: the next item's K tiles
+    if (has_next) {
+      if (tid == 32) load_k(nxt);
+      k_issued = li + 2;
     }
-    v_pending = true;
     gram_mma(1);
     wait_mma();
     SPLIT_MARK(6, mk);
 
-    // ---- Gram epilogue (warps 0-3) | (beta V)^T (warps 4-7) -----------------
+    // ---- Gram epilogue: diagonal halves (warps 0-3) | cross block (warps 4-7)
     float* s_akk = reinterpret_cast<float*>(smem + I_AKK);
+    const int l = tid & 127;  // TMEM lane
     if (warp < 4) {
-      const int l = tid;  // TMEM lane
       {  // diagonal halves: lane l holds row (l & 31) of q0 | k0 | q1 | k1
         const int part = l >> 5, rl = l & 31;
         const int hf = part >> 1, isk = part & 1;
@@ -395,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
       }
+    } else {
       {  // cross block (rows 32..63 x columns 0..31): product row m in lane
          // 32 (m / 16) + m % 16
         float v[32];
@@ -427,27 +496,11 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
         }
       }
-    } else {
-      // (beta V)^T, K-major [value channel jv][row r]
-      if (!sm100::mbar_wait(bar_v, 0)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
-      const int jv = tid - 128;
-      const unsigned char* sv = smem + I_V + (jv >> 6) * 8192;
-#pragma unroll
-      for (int g8 = 0; g8 < 8; ++g8) {
-        float t[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int r = 8 * g8 + e;
-          t[e] = (r < L) ? beta_at(r) * ld_bf16(sv, sw128_off(r, jv & 63)) : 0.0f;
-        }
-        st8_bf16(smem + I_BV + k64_off(jv, 8 * g8), t);
-      }
     }
     sm100::fence_async_smem();
     sync_all();
     SPLIT_MARK(7, mk);
     if (*s_abort) break;
-    v_pending = false;
 
     // ---- T = (I + beta A_kk)^{-1} -------------------------------------------
     unit_lower_inverse<AKK_LD>(s_akk, reinterpret_cast<float*>(smem + I_TF),
@@ -455,6 +508,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     sm100::fence_async_smem();
     sync_all();
     SPLIT_MARK(8, mk);
+    // the solve scratch (over V's landing zone) and beta are dead: the next
+    // item's V tiles and beta
+    if (has_next) {
+      if (tid == 32) load_v(nxt);
+      v_issued = li + 2;
+      beta_raw = load_beta(nxt);
+    }
 
     // ---- W^T = (beta K gamma)^T T^T and U = [T; -] (beta V) ------------------
     if (tid == 0) {
@@ -477,6 +537,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     wait_mma();
     SPLIT_MARK(9, mk);
     if (*s_abort) break;
+    // T (over Q) and (beta V)^T (over G) are dead: the next item's Q and G
+    if (has_next) {
+      if (tid == 32) load_qg(nxt);
+      qg_issued = li + 2;
+    }
 
     // ---- record: W rows (all warps: lane = key channel, 32 rows each) and
     //      U (warps 0, 1, 4, 5: lane = row, one value half each) -------------
@@ -509,14 +574,20 @@ __global__ void __launch_bounds__(kThreads, 2)
               make_float4(u[4 * q4], u[4 * q4 + 1], u[4 * q4 + 2], u[4 * q4 + 3]);
       }
     }
-  } while (0);
-  SPLIT_MARK(10, mk);
+    SPLIT_MARK(10, mk);
+#ifdef KDA_PHASE_TIMING
+    if (mk) atomicAdd(&kda_split_cycles[12], 1ull);  // items measured
+#endif
+    cur = nxt;
+  }
 
   // after an abort: bounded waits for copies and products still in flight
-  // before the shared and tensor memory are released
+  // before the shared and tensor memory are released (at most one copy per
+  // barrier is outstanding)
   if (*s_abort) {
-    if (in_pending) sm100::mbar_wait(bar_in, 0, 200000000ull);
-    if (v_pending) sm100::mbar_wait(bar_v, 0, 200000000ull);
+    if (qg_issued > qg_done) sm100::mbar_wait(bar_qg, qg_done & 1, 200000000ull);
+    if (k_issued > k_done) sm100::mbar_wait(bar_k, k_done & 1, 200000000ull);
+    if (v_issued > v_done) sm100::mbar_wait(bar_v, v_done & 1, 200000000ull);
     if (mma_pending) sm100::mbar_wait(bar_mma, mma_phase & 1, 200000000ull);
   }
   sm100::tc_fence_before();
@@ -656,33 +727,30 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
     SPLIT_MARK(17, mk);
 
     // (1) bf16 copy of S (B of the P product) and S <- gamma_C S ahead of the
-    //     rank-64 update (warps 0-3, lane = key channel) | output rows of the
-    //     previous chunk (warps 6-7)
-    if (warp < 4) {
-      const int i = tid;
+    //     rank-64 update (all warps: lane = key channel, 32 columns each)
+    {
+      const int i = tid & 127, cb = (warp >> 2) * 32;
       const float gc = reinterpret_cast<const float*>(st + ST_GC)[i];
-      float sv[64];
+      float sv[32];
 #pragma unroll
-      for (int c16 = 0; c16 < 64; c16 += 16) {
+      for (int c16 = 0; c16 < 32; c16 += 16) {
         float v[16];
-        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c16), v);
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + cb + c16), v);
 #pragma unroll
         for (int e = 0; e < 16; ++e) sv[c16 + e] = v[e];
       }
       sm100::tmem_wait_ld();
 #pragma unroll
-      for (int jg = 0; jg < 8; ++jg)
-        st8_bf16(smem + S_SB + mn_off(8 * jg, i, 1024), sv + 8 * jg);
+      for (int jg = 0; jg < 4; ++jg)
+        st8_bf16(smem + S_SB + mn_off(cb + 8 * jg, i, 1024), sv + 8 * jg);
 #pragma unroll
-      for (int c16 = 0; c16 < 64; c16 += 16) {
+      for (int c16 = 0; c16 < 32; c16 += 16) {
         uint32_t r[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(gc * sv[c16 + e]);
-        sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + c16), r);
+        sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + cb + c16), r);
       }
       sm100::tmem_wait_st();
-    } else if (warp >= 6 && c > 0) {
-      write_out(c - 1);
     }
     sm100::fence_async_smem();
     sync_all();
@@ -701,6 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
       sm100::mma_commit(bar_mma);
     }
     mma_pending = true;
+    // output rows of the previous chunk while the tensor cores work on P
+    if (warp >= 6 && c > 0) write_out(c - 1);
     wait_mma();
     SPLIT_MARK(19, mk);
 
@@ -867,6 +937,10 @@ kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_
   if (workspace_bytes < carry + per) return KDA_ERR_WORKSPACE;
   const int nchunks = (int)(((int64_t)p.T + C - 1) / C);
   const size_t fit = (workspace_bytes - carry) / per;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return KDA_ERR_CUDA;
   const int slice = fit < (size_t)nchunks ? (int)fit : nchunks;
   if (one_slice && slice < nchunks) return KDA_ERR_WORKSPACE;
   CUtensorMap mq, mk, mg, mv;
@@ -898,8 +972,10 @@ kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_
     sp.s_in = c0 == 0 ? p.init_state : through;
     sp.s_out = last ? p.final_state : through;
     if (stages & 1) {
-      kda_tc_intra_kernel<<<dim3(cnt, p.H, p.N), kThreads, I_SMEM, stream>>>(mq, mk, mg, mv,
-                                                                              sp);
+      // persistent: two CTAs per SM walk the slice's (sequence, head, chunk) items
+      const int64_t items = (int64_t)p.N * p.H * cnt;
+      const int grid = items < 2 * (int64_t)sms ? (int)items : 2 * sms;
+      kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(mq, mk, mg, mv, sp);
       if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
     }
     if (stages & 2) {

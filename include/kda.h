@@ -80,7 +80,8 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
 /* Implementation choice for kda_chunk_fwd_ex (the result is the same
  * function of the inputs up to rounding). */
 typedef enum {
-  KDA_ALGO_AUTO = 0,  /* tensor-core path where built, else CUDA-core path */
+  KDA_ALGO_AUTO = 0,  /* tensor-core path where built (two-kernel form for dense
+                       * batches, fused kernel for packed ones), else CUDA-core */
   KDA_ALGO_SIMT = 1,  /* fp32 CUDA-core chunked path (16-token chunks) */
   KDA_ALGO_TC = 2,    /* tcgen05/TMEM/TMA fused path (bf16, dk = dv = 128) */
   KDA_ALGO_SPLIT = 3  /* tensor-core path in two kernels (bf16, dk = dv = 128, dense
@@ -236,7 +237,8 @@ kda_status kda_chunk_fwd_host(const void* q, const void* k, const void* v, const
                               const int32_t* cu_seqlens, kda_dtype dtype, float scale,
                               void* dev_buffer, size_t dev_buffer_bytes, kda_stream_t stream);
 
-/* Device bytes kda_chunk_fwd_host stages through for these sizes. */
+/* Device bytes kda_chunk_fwd_host stages through for these sizes: inputs,
+ * outputs, states and the automatic path's workspace. */
 size_t kda_host_staging_bytes(int B, int T, int H, int dk, int dv, int dtype, int has_init,
                               int has_final, int packed);
 

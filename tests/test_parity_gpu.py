@@ -15,7 +15,9 @@ from kda_inputs import WORKLOADS, make_inputs, make_unit, small_workload
 pytestmark = pytest.mark.gpu
 
 TOL = {torch.bfloat16: 1e-2, torch.float32: 1e-4}
-ALGOS = [kda.KDA_ALGO_SIMT, kda.KDA_ALGO_AUTO]
+# AUTO: the two-kernel tensor-core path on dense batches, the fused kernel on
+# packed ones; TC: the fused kernel on both
+ALGOS = [kda.KDA_ALGO_SIMT, kda.KDA_ALGO_AUTO, kda.KDA_ALGO_TC]
 
 
 def rel(a, ref):
@@ -229,7 +231,9 @@ def _sampled_check(name, units, algo=kda.KDA_ALGO_AUTO):
 
 
 def test_full_b2_h32_t32k_sampled():
-    _sampled_check("b2_h32_t32k", [(0, 0), (1, 31), (0, 17), (1, 5)])
+    # the fused kernel at full size (the automatic path's two-kernel form is
+    # checked at full size in test_split_gpu.py)
+    _sampled_check("b2_h32_t32k", [(0, 0), (1, 31), (0, 17), (1, 5)], algo=kda.KDA_ALGO_TC)
 
 
 def test_full_varlen_floor_sampled():
