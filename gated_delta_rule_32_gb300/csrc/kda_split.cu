@@ -832,19 +832,21 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
       issued = c + 3;
     }
 
-    // (5) state checkpoint (warps 0-3, lane = key channel)
-    if (p.ckpt && warp < 4) {
+    // (5) state checkpoint (all warps: lane = key channel, the 32 columns
+    //     this warp rescales next, so program order alone keeps the read
+    //     ahead of the next chunk's rescaling)
+    if (p.ckpt) {
       const int64_t cs = ((int64_t)sp.c_begin + c) * C;
       const int L = (p.T - cs) < C ? (int)(p.T - cs) : C;
       const int64_t done = cs + L;
       if (L == C && done % p.ckpt_every == 0 && done / p.ckpt_every <= p.ckpt_max) {
-        const int i = tid;
+        const int i = tid & 127, cb = (warp >> 2) * 32;
         float* dst = p.ckpt + ((((int64_t)n * H + h) * p.ckpt_max + done / p.ckpt_every - 1) *
-                                   DK + i) * DV + half * 64;
+                                   DK + i) * DV + half * 64 + cb;
 #pragma unroll
-        for (int c16 = 0; c16 < 64; c16 += 16) {
+        for (int c16 = 0; c16 < 32; c16 += 16) {
           float v[16];
-          sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c16), v);
+          sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + cb + c16), v);
           sm100::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 16; e += 4)

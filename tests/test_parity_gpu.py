@@ -93,6 +93,8 @@ def test_ragged_d128_bf16(algo, T):
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_varlen_edge_lengths(algo, dtype):
+    if dtype == torch.float32 and algo == kda.KDA_ALGO_TC:
+        pytest.skip("the fused tensor-core kernel takes bf16 inputs")
     lens = (1, 15, 16, 17, 63, 64, 65, 130)
     w = small_workload("v", B=1, T=sum(lens), H=2, dk=128, dv=128, dtype=dtype, seed=9,
                        varlen=True, lengths=lens, s0_std=0.03)
