@@ -309,22 +309,25 @@ def run_ours(args):
     value = ws * tokens / (ms_per_step / 1e3)
 
     # ---- the two kernels of the split path, each timed alone ----------------
-    split = (dtype == kda.KDA_BF16 and dk == 128 and dv == 128 and not w.varlen and T > 0 and
-             args.algo in (kda.KDA_ALGO_AUTO, kda.KDA_ALGO_SPLIT))
+    path = kda.kda_resolve_path(N, T, H, dk, dv, dtype, 0, args.algo, w.varlen)
+    split = path == kda.KDA_ALGO_SPLIT
     launches_per_step = 1
     split_ms = {}
     if split:
         rec = 90624  # bytes of one chunk record
+        sws = ws_bytes
         carry = (N * H * dk * dv * 4 + 255) // 256 * 256
-        slice_chunks = (ws_bytes - carry) // (N * H * rec)
         nchunks = (T + 63) // 64
+        slice_chunks = (ws_bytes - carry) // (N * H * rec)
         launches_per_step = 2 * ((nchunks + slice_chunks - 1) // slice_chunks)
+        swork = work
+        one_slice = slice_chunks >= nchunks
 
         def stage(sg):
             return kda.kda_split_stage(sg, d["q"], d["k"], d["v"], d["g"], d["beta"],
-                                       d["init_state"], out, fs, N, T, H, 1.0, work, ws_bytes,
+                                       d["init_state"], out, fs, N, T, H, 1.0, swork, sws,
                                        None, stream)
-        if launches_per_step == 2 and stage(1) == 0 and stage(2) == 0:
+        if one_slice and stage(1) == 0 and stage(2) == 0:
             n_k = max(3, args.steps)
             for sg, name in ((1, "kda_tc_intra_kernel"), (2, "kda_tc_state_kernel")):
                 e0 = torch.cuda.Event(enable_timing=True)
@@ -377,7 +380,6 @@ def run_ours(args):
         return 0
 
     hbm_gbs, bf16_tf, peak_src = measured_peaks()
-    path = kda.kda_resolve_algo(dtype, dk, dv, 0, args.algo)
     kname = "kda_tc_fused_kernel" if path == kda.KDA_ALGO_TC else "kda_simt_kernel"
     traffic = None
     kernels = None

@@ -109,7 +109,6 @@ kda_status kda_run_split(const kda::FwdParams& p, void* workspace, size_t worksp
                          cudaStream_t stream);
 size_t kda_split_workspace_bytes(int N, int T, int H);
 size_t kda_split_min_workspace_bytes(int N, int H);
-
 // A workspace smaller than the default (but at least the minimum) runs the
 // sequence in more, shorter slices.
 static kda_status run_split_ws(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
@@ -170,6 +169,16 @@ int kda_resolve_algo(int dtype, int dk, int dv, int chunk_size, int algo) {
   if ((algo == KDA_ALGO_TC || algo == KDA_ALGO_SPLIT) && !tc) return -1;
   if (algo == KDA_ALGO_SPLIT) return KDA_ALGO_SPLIT;
   return tc ? KDA_ALGO_TC : KDA_ALGO_SIMT;
+}
+
+int kda_resolve_path(int N, int T, int H, int dk, int dv, int dtype, int chunk_size, int algo,
+                     int packed) {
+  const int fam = kda_resolve_algo(dtype, dk, dv, chunk_size, algo);
+  if (fam < 0 || N < 1 || H < 1 || T < 0) return -1;
+  if (fam == KDA_ALGO_SIMT) return KDA_ALGO_SIMT;
+  if (algo == KDA_ALGO_TC) return KDA_ALGO_TC;
+  if (!use_split(dtype, dk, dv, chunk_size, algo, packed, T)) return KDA_ALGO_TC;
+  return KDA_ALGO_SPLIT;
 }
 
 size_t kda_workspace_bytes(int N, int T, int H, int dk, int dv, int dtype, int chunk_size,

@@ -674,10 +674,15 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
   bool mma_pending = false;
   int issued = nc < 2 ? nc : 2;  // chunks whose record copy has been issued
   int landed = 0;                 // chunks whose record copy has been waited for
+  // one thread waits for the products; the others meet it at the barrier
   auto wait_mma = [&]() {
-    const bool ok = sm100::mbar_wait(bar_mma, mma_phase & 1);
+    bool ok1 = true;
+    if (tid == 0) {
+      ok1 = sm100::mbar_wait(bar_mma, mma_phase & 1);
+      if (!ok1) record_error(p, s_abort, KDA_ERR_TIMEOUT);
+    }
+    const bool ok = __syncthreads_and(ok1);
     if (ok) ++mma_phase;
-    else record_error(p, s_abort, KDA_ERR_TIMEOUT);
     mma_pending = !ok;
     sm100::tc_fence_after();
   };

@@ -40,6 +40,7 @@ _SIGS = {
     "kda_status_string": (ctypes.c_char_p, [_i]),
     "kda_build_info": (ctypes.c_char_p, []),
     "kda_resolve_algo": (_i, [_i] * 5),
+    "kda_resolve_path": (_i, [_i] * 9),
     "kda_chunk_fwd": (_i, [_vp] * 8 + [_i] * 5 + [_vp, _vp]),
     "kda_chunk_fwd_f32": (_i, [_vp] * 8 + [_i] * 5 + [_vp, _vp]),
     "kda_chunk_fwd_ex": (_i, [_vp] * 8 + [_i] * 5 + [_vp, _i, _i, ctypes.c_float, _i, _vp,
@@ -116,6 +117,11 @@ def status_string(code: int) -> str:
 
 def kda_build_info() -> str:
     return load().kda_build_info().decode()
+
+
+def kda_resolve_path(N, T, H, dk=128, dv=128, dtype=KDA_BF16, chunk_size=0,
+                     algo=KDA_ALGO_AUTO, packed=False) -> int:
+    return load().kda_resolve_path(N, T, H, dk, dv, dtype, chunk_size, algo, int(packed))
 
 
 def kda_resolve_algo(dtype=KDA_BF16, dk=128, dv=128, chunk_size=0, algo=KDA_ALGO_AUTO) -> int:

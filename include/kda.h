@@ -296,6 +296,12 @@ kda_status kda_split_stage(int stage, const uint16_t* q, const uint16_t* k, cons
  * combination is unsupported. */
 int kda_resolve_algo(int dtype, int dk, int dv, int chunk_size, int algo);
 
+/* The path kda_chunk_fwd_ex takes for these sizes (N sequences, T tokens per
+ * row, or in total when packed): KDA_ALGO_SIMT, KDA_ALGO_TC (fused kernel)
+ * or KDA_ALGO_SPLIT; -1 if the call would be refused. */
+int kda_resolve_path(int N, int T, int H, int dk, int dv, int dtype, int chunk_size, int algo,
+                     int packed);
+
 /* Library build identification (static string). */
 const char* kda_build_info(void);
 

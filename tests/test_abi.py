@@ -118,3 +118,16 @@ def test_split_path_host_checks(lib):
     assert kda.kda_split_stage(1, **dict(st, workspace=None)) == kda.KDA_ERR_INVALID_ARG
     assert kda.kda_split_stage(1, **dict(st, q=A + 8)) == kda.KDA_ERR_MISALIGNED
     assert kda.kda_split_stage(2, **dict(st, T=0)) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_resolve_path(lib):
+    # the automatic path of a dense bf16 batch is the two-kernel form, packed
+    # batches take the fused kernel, fp32 inputs the CUDA-core path
+    rp = kda.kda_resolve_path
+    assert rp(2, 32768, 32) == kda.KDA_ALGO_SPLIT
+    assert rp(2, 32768, 32, packed=True) == kda.KDA_ALGO_TC
+    assert rp(2, 32768, 32, algo=kda.KDA_ALGO_TC) == kda.KDA_ALGO_TC
+    assert rp(2, 100, 4, dtype=kda.KDA_F32) == kda.KDA_ALGO_SIMT
+    assert rp(2, 100, 4, dk=64) == kda.KDA_ALGO_SIMT
+    assert rp(0, 100, 4) == -1
+    assert rp(2, 100, 4, dtype=kda.KDA_F32, algo=kda.KDA_ALGO_SPLIT) == -1
