@@ -125,20 +125,44 @@ __global__ void __launch_bounds__(kThreads, 2)
   // takes blockIdx.x, blockIdx.x + gridDim.x, ...
   const int64_t n_items = (int64_t)p.N * H * sp.c_count;
   struct Item {
-    int h;
+    int n, h, cl;    // sequence, head, chunk of the slice
     int L;           // valid rows of the chunk
     int64_t row0;    // global row of its first token
     int64_t w;
   };
+  auto finish = [&](Item& it) {
+    const int64_t cs = ((int64_t)sp.c_begin + it.cl) * C;
+    it.L = (p.T - cs) < C ? (int)(p.T - cs) : C;
+    it.row0 = (int64_t)it.n * p.T + cs;
+  };
+  // the coordinates of item w (divisions: once per CTA), and those of the
+  // item gridDim.x further on, by carries (32-bit adds only)
   auto item_of = [&](int64_t w) {
     Item it;
-    const int64_t nh = w / sp.c_count, cl = w % sp.c_count;
-    it.h = (int)(nh % H);
-    const int64_t n = nh / H;
-    const int64_t cs = ((int64_t)sp.c_begin + cl) * C;
-    it.L = (p.T - cs) < C ? (int)(p.T - cs) : C;
-    it.row0 = n * p.T + cs;
+    const int nh = (int)(w / sp.c_count);
+    it.cl = (int)(w % sp.c_count);
+    it.h = nh % H;
+    it.n = nh / H;
     it.w = w;
+    finish(it);
+    return it;
+  };
+  const int step_cl = (int)(gridDim.x % sp.c_count);
+  const int step_nh = (int)(gridDim.x / sp.c_count);
+  const int step_h = step_nh % H, step_n = step_nh / H;
+  auto next_of = [&](const Item& a) {
+    Item it;
+    it.w = a.w + gridDim.x;
+    it.cl = a.cl + step_cl;
+    const int carry = it.cl >= sp.c_count;
+    if (carry) it.cl -= sp.c_count;
+    it.h = a.h + step_h + carry;
+    it.n = a.n + step_n;
+    if (it.h >= H) {
+      it.h -= H;
+      it.n += 1;
+    }
+    finish(it);
     return it;
   };
 #ifdef KDA_PHASE_TIMING
@@ -230,12 +254,24 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int li = 0; cur.w < n_items; ++li) {
     const int L = cur.L;
     unsigned char* rec = sp.rec + cur.w * (int64_t)REC_BYTES;
-    const Item nxt = item_of(cur.w + gridDim.x);
+    const Item nxt = next_of(cur);
     const bool has_next = nxt.w < n_items;
     const uint32_t par = (uint32_t)(li & 1);
     if (!sm100::mbar_wait(bar_qg, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
     else qg_done = li + 1;
     if (tid < C) s_beta_raw[tid] = beta_raw;  // bf16 bits; readers widen them
+    // rows past the end of the sequence (its last chunk only): q = 0 and a
+    // decay logit far below zero (alpha = 1), so that no later step masks
+    if (L < C) {
+      for (int e = tid; e < (C - L) * 16; e += kThreads) {
+        const int r = L + (e >> 4), box = (e >> 3) & 1, piece = e & 7;
+        const uint32_t off = box * 8192 + r * 128 + piece * 16;
+        *reinterpret_cast<uint4*>(smem + I_Q + off) = make_uint4(0, 0, 0, 0);
+        const uint32_t ng = 0xC61CC61Cu;  // bf16 pair (-9984, -9984)
+        *reinterpret_cast<uint4*>(smem + I_G + off) = make_uint4(ng, ng, ng, ng);
+      }
+      __syncthreads();
+    }
     SPLIT_MARK(1, mk);
 
     // ---- gate, pass 0: decay factors of 16 rows (tile a) of key channels
@@ -250,8 +286,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int s = 0; s < 16; ++s) {
         const int r = 16 * a + s;
         const uint32_t o = sw128_off(r, jl);
-        al0[s] = r < L ? alpha_of(ld_bf16(g0, o)) : 1.0f;
-        al1[s] = r < L ? alpha_of(ld_bf16(g1, o)) : 1.0f;
+        al0[s] = alpha_of(ld_bf16(g0, o));
+        al1[s] = alpha_of(ld_bf16(g1, o));
         p0 *= al0[s];
         p1 *= al1[s];
       }
@@ -306,6 +342,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float cf = tt == 0 ? 1.0f : invPb;   // diagonal-half column factor
       // cross-block factor: column (first half) or row (second half)
       const float xf = pr == 0 ? (tt == 0 ? P1 : 1.0f) : (tt == 0 ? 1.0f : P2);
+      // q's factors carry the scale
+      const float rsq = rs * p.scale, xfq = xf * p.scale, preq = pre * p.scale;
       float F[16];
       {
         float f = 1.0f;
@@ -321,9 +359,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int e8 = 0; e8 < 8; ++e8) {
           const int r = r0 + e8;
           const uint32_t o = sw128_off(r, jl);
-          const bool ok = r < L;
-          const float qv = ok ? ld_bf16(sq, o) * p.scale : 0.0f;
-          const float kv = ok ? ld_bf16(sk, o) : 0.0f;
+          const float qv = ld_bf16(sq, o);
+          const float kv = ld_bf16(sk, o);
           e *= al[8 * g + e8];
           qE[e8] = qv * e;
           kE[e8] = kv * e;
@@ -331,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (pr == 0) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) t[i] = qE[i] * rs;
+          for (int i = 0; i < 8; ++i) t[i] = qE[i] * rsq;
           st8_bf16(smem + I_A1 + mn_off(r0, jl, 2048), t);
 #pragma unroll
           for (int i = 0; i < 8; ++i) t[i] = kE[i] * rs;
@@ -345,13 +382,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         } else {
           const int rr0 = r0 - 32;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) t[i] = qE[i] * rs;
+          for (int i = 0; i < 8; ++i) t[i] = qE[i] * rsq;
           st8_bf16(smem + I_A1 + mn_off(64 + rr0, jl, 2048), t);
 #pragma unroll
           for (int i = 0; i < 8; ++i) t[i] = kE[i] * rs;
           st8_bf16(smem + I_A1 + mn_off(96 + rr0, jl, 2048), t);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) t[i] = qE[i] * xf;
+          for (int i = 0; i < 8; ++i) t[i] = qE[i] * xfq;
           st8_bf16(smem + I_A2 + mn_off(rr0, jl, 1024), t);
 #pragma unroll
           for (int i = 0; i < 8; ++i) t[i] = kE[i] * xf;
@@ -362,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         // Q gamma into rows 64.. of the record's [W; Q gamma]
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = qE[i] * pre;
+        for (int i = 0; i < 8; ++i) t[i] = qE[i] * preq;
         st8_bf16(rec + REC_WQ + mn_off(64 + r0, j, 2048), t);
         // (beta K gamma)^T, K-major [j][r]
 #pragma unroll
@@ -397,6 +434,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     if (!sm100::mbar_wait(bar_k, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
     else k_done = li + 1;
+    if (L < C) {  // k = 0 past the end of the sequence
+      for (int e = tid; e < (C - L) * 16; e += kThreads) {
+        const int r = L + (e >> 4), box = (e >> 3) & 1, piece = e & 7;
+        *reinterpret_cast<uint4*>(smem + I_K + box * 8192 + r * 128 + piece * 16) =
+            make_uint4(0, 0, 0, 0);
+      }
+      __syncthreads();
+    }
     gate_pass(al0, 0);
     sm100::fence_async_smem();
     sync_all();
