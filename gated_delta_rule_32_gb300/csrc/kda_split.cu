@@ -7,16 +7,19 @@
 // S <- gamma_C S + (K dec)^T Delta chain one chunk to the next (Towards AI
 // walkthrough, "Infrastructure co-design": the chunk-to-chunk state
 // dependency is the only serial part).  So:
-//   intra kernel  one CTA per (chunk, head, sequence), every chunk at once,
-//                 two CTAs per SM; writes one record per chunk to global
+//   intra kernel  persistent, two CTAs per SM walking the (sequence, head,
+//                 chunk) items; writes one record per chunk to global
 //                 memory, laid out as the state kernel's shared-memory image;
 //   state kernel  one CTA per (half of the value channels, head, sequence);
-//                 per chunk a bulk copy of the record, two tensor-core
-//                 products and two short epilogues, the state in tensor
-//                 memory throughout.
+//                 per chunk a bulk copy of the record, the U product of its
+//                 half (off the chain: it runs while the CUDA cores copy the
+//                 state), then two tensor-core products and two short
+//                 epilogues on the chain, the state in tensor memory
+//                 throughout.
 // The record holds the operands in the precision the fused kernel feeds its
-// own state products (bf16 W, Q gamma, K dec, A_qk; fp32 U, gamma_C), so the
-// two paths round at the same points.
+// own products (bf16 W, Q gamma, K dec, A_qk, T, beta V; fp32 gamma_C), and
+// U is accumulated in fp32 from the same bf16 T and beta V, so the two paths
+// round at the same points.
 //
 // A long sequence runs in slices of chunks (intra kernel over the slice,
 // then the state kernel over it), so the record buffer stays bounded; the
@@ -40,12 +43,18 @@ constexpr int AKK_LD = 72;
 constexpr int REC_KD = 0;        // (K dec)^T, K-major [key channel j][row r]  16384
 constexpr int REC_AQ = 16384;    // A_qk masked (i <= r), K-major [r][i]         8192
 constexpr int REC_WQ = 24576;    // [W; Q gamma], MN-major 128 rows x 128 K     32768
-constexpr int REC_U = 57344;     // U fp32 [value half][c / 4][r][4]            32768
-constexpr int REC_GC = 90112;    // gamma_C fp32 [128]                             512
-constexpr int REC_BYTES = 90624;
-// the part of a record one state CTA copies: KD | AQ | WQ, its U half, gamma_C
-constexpr int ST_KD = 0, ST_AQ = 16384, ST_WQ = 24576, ST_U = 57344, ST_GC = 73728;
+constexpr int REC_T = 57344;     // T = (I + beta A_kk)^-1, K-major [r][i]       8192
+constexpr int REC_BV = 65536;    // (beta V)^T, K-major [value channel][r]      16384
+constexpr int REC_GC = 81920;    // gamma_C fp32 [128]                             512
+constexpr int REC_BYTES = 82432;
+// the part of a record one state CTA copies: KD | AQ | WQ | T, the (beta V)^T
+// rows of its value half, gamma_C.  U = T (beta V) of the half is formed
+// there, on the tensor cores, into tensor memory: its rows past 63 read the
+// (beta V)^T rows that follow T and are never used.
+constexpr int ST_KD = 0, ST_AQ = 16384, ST_WQ = 24576, ST_T = 57344, ST_BV = 65536,
+              ST_GC = 73728;
 constexpr int STAGE_BYTES = 74240;
+static_assert(ST_BV == ST_T + 8192 && REC_BV == REC_T + 8192, "U operand rows");
 
 struct SplitParams {
   kda::FwdParams p;
@@ -98,19 +107,15 @@ constexpr int I_SMEM = I_MISC + 64;
 // V lands with Q, K, G in the Gram operand buffer, which is free until the
 // first gate pass; the rest overlays what is dead by then
 constexpr int I_V = I_OB;                          // V landing, 2 boxes (until (beta V)^T)
-constexpr int I_BV = I_G;                          // (beta V)^T K-major [jv][r] 128 x 64
 constexpr int I_AKK = I_OB, I_TF = I_OB + 18432;   // [64][72] fp32 each (after the Grams)
 constexpr int I_T = I_Q, I_Y = I_Q + 8192;         // T bf16 (8192), Y fp32 [32][36]
 static_assert(I_V + 16384 <= I_BKG, "V landing");
 static_assert(I_TF + 64 * AKK_LD * 4 <= I_BKG, "solve scratch");
 static_assert(I_Y + 32 * 36 * 4 <= I_K, "block-merge scratch");
-// the U product reads 128 rows [T; -] from I_T: they stay inside the Q region
-static_assert(I_T + 16384 <= I_K, "U operand rows");
 static_assert(2 * (I_SMEM + 1024) <= 233472, "two CTAs per SM");
-constexpr uint32_t I_TM_COLS = 256;
+constexpr uint32_t I_TM_COLS = 128;
 constexpr uint32_t TM_G = 0;     // Gram products: [0, 64) diagonal halves, [64, 96) cross
 constexpr uint32_t TM_W = 0;     // W^T (after the Grams are read)
-constexpr uint32_t TM_U = 64;    // U, 128 columns
 
 __global__ void __launch_bounds__(kThreads, 2)
     kda_tc_intra_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -119,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         const __grid_constant__ CUtensorMap tm_v, const SplitParams sp) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const kda::FwdParams& p = sp.p;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int H = p.H;
   // work items: w = (n * H + h) * c_count + chunk of the slice; this CTA
   // takes blockIdx.x, blockIdx.x + gridDim.x, ...
@@ -170,10 +175,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   const bool mk = tid == 0 && blockIdx.x == 0;
 #endif
 
-  uint64_t* bar_qg = reinterpret_cast<uint64_t*>(smem + I_BAR);  // Q and G tiles
-  uint64_t* bar_k = bar_qg + 1;                                   // K tiles
-  uint64_t* bar_v = bar_qg + 2;                                   // V tiles
-  uint64_t* bar_mma = bar_qg + 3;
+  uint64_t* bar_q = reinterpret_cast<uint64_t*>(smem + I_BAR);  // Q tiles
+  uint64_t* bar_g = bar_q + 1;                                   // decay-logit tiles
+  uint64_t* bar_k = bar_q + 2;                                   // K tiles
+  uint64_t* bar_v = bar_q + 3;                                   // V tiles
+  uint64_t* bar_mma = bar_q + 4;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + I_MISC);
   int* s_abort = reinterpret_cast<int*>(smem + I_MISC + 4);
   unsigned short* s_beta_raw = reinterpret_cast<unsigned short*>(smem + I_BETA);
@@ -186,13 +192,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   // the tiles of an item land region by region as the previous item's use
   // of that region ends (issued by thread 32)
-  auto load_qg = [&](const Item& it) {
-    const int row = (int)it.row0;
-    sm100::mbar_arrive_expect_tx(bar_qg, 32768);
-    sm100::tma_load_3d(smem + I_Q, &tm_q, bar_qg, 0, it.h, row);
-    sm100::tma_load_3d(smem + I_Q + 8192, &tm_q, bar_qg, 64, it.h, row);
-    sm100::tma_load_3d(smem + I_G, &tm_g, bar_qg, 0, it.h, row);
-    sm100::tma_load_3d(smem + I_G + 8192, &tm_g, bar_qg, 64, it.h, row);
+  auto load_q = [&](const Item& it) {
+    sm100::mbar_arrive_expect_tx(bar_q, 16384);
+    sm100::tma_load_3d(smem + I_Q, &tm_q, bar_q, 0, it.h, (int)it.row0);
+    sm100::tma_load_3d(smem + I_Q + 8192, &tm_q, bar_q, 64, it.h, (int)it.row0);
+  };
+  auto load_g = [&](const Item& it) {
+    sm100::mbar_arrive_expect_tx(bar_g, 16384);
+    sm100::tma_load_3d(smem + I_G, &tm_g, bar_g, 0, it.h, (int)it.row0);
+    sm100::tma_load_3d(smem + I_G + 8192, &tm_g, bar_g, 64, it.h, (int)it.row0);
   };
   auto load_k = [&](const Item& it) {
     sm100::mbar_arrive_expect_tx(bar_k, 16384);
@@ -212,13 +220,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
   Item cur = item_of(blockIdx.x);
   if (tid == 32) {
-    sm100::mbar_init(bar_qg, 1);
+    sm100::mbar_init(bar_q, 1);
+    sm100::mbar_init(bar_g, 1);
     sm100::mbar_init(bar_k, 1);
     sm100::mbar_init(bar_v, 1);
     sm100::mbar_init(bar_mma, 1);
     sm100::fence_mbar_init();
     if (cur.w < n_items) {
-      load_qg(cur);
+      load_g(cur);
+      load_q(cur);
       load_k(cur);
       load_v(cur);
     }
@@ -236,8 +246,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint32_t mma_phase = 0;
   // items whose copies were issued / waited for, per barrier
   const int first = cur.w < n_items ? 1 : 0;
-  int qg_issued = first, k_issued = first, v_issued = first;
-  int qg_done = 0, k_done = 0, v_done = 0;
+  int q_issued = first, g_issued = first, k_issued = first, v_issued = first;
+  int q_done = 0, g_done = 0, k_done = 0, v_done = 0;
   auto wait_mma = [&]() {
     const bool ok = sm100::mbar_wait(bar_mma, mma_phase & 1);
     if (ok) ++mma_phase;
@@ -257,18 +267,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     const Item nxt = next_of(cur);
     const bool has_next = nxt.w < n_items;
     const uint32_t par = (uint32_t)(li & 1);
-    if (!sm100::mbar_wait(bar_qg, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
-    else qg_done = li + 1;
+    if (!sm100::mbar_wait(bar_g, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
+    else g_done = li + 1;
     if (tid < C) s_beta_raw[tid] = beta_raw;  // bf16 bits; readers widen them
-    // rows past the end of the sequence (its last chunk only): q = 0 and a
-    // decay logit far below zero (alpha = 1), so that no later step masks
+    // rows past the end of the sequence (its last chunk only): a decay logit
+    // far below zero (alpha = 1), so that no later step masks
     if (L < C) {
       for (int e = tid; e < (C - L) * 16; e += kThreads) {
         const int r = L + (e >> 4), box = (e >> 3) & 1, piece = e & 7;
-        const uint32_t off = box * 8192 + r * 128 + piece * 16;
-        *reinterpret_cast<uint4*>(smem + I_Q + off) = make_uint4(0, 0, 0, 0);
         const uint32_t ng = 0xC61CC61Cu;  // bf16 pair (-9984, -9984)
-        *reinterpret_cast<uint4*>(smem + I_G + off) = make_uint4(ng, ng, ng, ng);
+        *reinterpret_cast<uint4*>(smem + I_G + box * 8192 + r * 128 + piece * 16) =
+            make_uint4(ng, ng, ng, ng);
       }
       __syncthreads();
     }
@@ -294,10 +303,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       s_pt[a * 128 + jl] = p0;
       s_pt[a * 128 + 64 + jl] = p1;
     }
+    sm100::fence_async_smem();
     __syncthreads();
     if (*s_abort) break;
-    // (beta V)^T, K-major [value channel jv][row r], over the dead G tiles;
-    // V is read before the gate passes overwrite it
+    // the decay logits live on in registers only: the next item's G tiles
+    if (has_next) {
+      if (tid == 32) load_g(nxt);
+      g_issued = li + 2;
+    }
+    // (beta V)^T, K-major [value channel jv][row r], into the record; V is
+    // read before the gate passes overwrite it
     if (!sm100::mbar_wait(bar_v, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
     else v_done = li + 1;
     {
@@ -311,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           const int r = 32 * rh + 8 * g8 + e;
           t[e] = (r < L) ? beta_at(r) * ld_bf16(sv, sw128_off(r, jv & 63)) : 0.0f;
         }
-        st8_bf16(smem + I_BV + k64_off(jv, 32 * rh + 8 * g8), t);
+        st8_bf16(rec + REC_BV + k64_off(jv, 32 * rh + 8 * g8), t);
       }
     }
     __syncthreads();
@@ -432,13 +447,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       mma_pending = true;
     };
 
+    if (!sm100::mbar_wait(bar_q, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
+    else q_done = li + 1;
     if (!sm100::mbar_wait(bar_k, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
     else k_done = li + 1;
-    if (L < C) {  // k = 0 past the end of the sequence
+    if (L < C) {  // q = k = 0 past the end of the sequence
       for (int e = tid; e < (C - L) * 16; e += kThreads) {
         const int r = L + (e >> 4), box = (e >> 3) & 1, piece = e & 7;
-        *reinterpret_cast<uint4*>(smem + I_K + box * 8192 + r * 128 + piece * 16) =
-            make_uint4(0, 0, 0, 0);
+        const uint32_t off = box * 8192 + r * 128 + piece * 16;
+        *reinterpret_cast<uint4*>(smem + I_Q + off) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(smem + I_K + off) = make_uint4(0, 0, 0, 0);
       }
       __syncthreads();
     }
@@ -549,7 +567,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ---- T = (I + beta A_kk)^{-1} -------------------------------------------
     unit_lower_inverse<AKK_LD>(s_akk, reinterpret_cast<float*>(smem + I_TF),
-                               reinterpret_cast<float*>(smem + I_Y), smem + I_T, tid);
+                               reinterpret_cast<float*>(smem + I_Y), smem + I_T, tid,
+                               rec + REC_T);
     sm100::fence_async_smem();
     sync_all();
     SPLIT_MARK(8, mk);
@@ -561,35 +580,29 @@ __global__ void __launch_bounds__(kThreads, 2)
       beta_raw = load_beta(nxt);
     }
 
-    // ---- W^T = (beta K gamma)^T T^T and U = [T; -] (beta V) ------------------
+    // ---- W^T = (beta K gamma)^T T^T (U = T (beta V) is formed by the state
+    //      kernel from the record's T and (beta V)^T) ------------------------
     if (tid == 0) {
       const uint32_t idw = sm100::idesc_bf16(128, 64, 0, 0);
-      const uint32_t idu = sm100::idesc_bf16(128, 128, 0, 0);
       const uint32_t s_bkg = sm100::smem_u32(smem + I_BKG);
       const uint32_t s_t = sm100::smem_u32(smem + I_T);
-      const uint32_t s_bv = sm100::smem_u32(smem + I_BV);
 #pragma unroll
       for (int s = 0; s < C / 16; ++s)
         sm100::mma_ss(tmem + TM_W, sm100::smem_desc(s_bkg + 256 * s, 128, 1024),
                       sm100::smem_desc(s_t + 256 * s, 128, 1024), idw, s > 0);
-#pragma unroll
-      for (int s = 0; s < C / 16; ++s)
-        sm100::mma_ss(tmem + TM_U, sm100::smem_desc(s_t + 256 * s, 128, 1024),
-                      sm100::smem_desc(s_bv + 256 * s, 128, 1024), idu, s > 0);
       sm100::mma_commit(bar_mma);
     }
     mma_pending = true;
     wait_mma();
     SPLIT_MARK(9, mk);
     if (*s_abort) break;
-    // T (over Q) and (beta V)^T (over G) are dead: the next item's Q and G
+    // T (over Q) is dead: the next item's Q tiles
     if (has_next) {
-      if (tid == 32) load_qg(nxt);
-      qg_issued = li + 2;
+      if (tid == 32) load_q(nxt);
+      q_issued = li + 2;
     }
 
-    // ---- record: W rows (all warps: lane = key channel, 32 rows each) and
-    //      U (warps 0, 1, 4, 5: lane = row, one value half each) -------------
+    // ---- record: W rows (all warps: lane = key channel, 32 rows each) -----
     {
       const int j = tid & 127, rb = (warp >> 2) * 32;
       float wv[32];
@@ -605,20 +618,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int rg = 0; rg < 4; ++rg)
         st8_bf16(rec + REC_WQ + mn_off(rb + 8 * rg, j, 2048), wv + 8 * rg);
     }
-    if ((warp & 3) < 2) {
-      const int r = (warp & 1) * 32 + lane, hf = warp >> 2;
-      float4* dst = reinterpret_cast<float4*>(rec + REC_U + hf * 16384);
-#pragma unroll
-      for (int c = 0; c < 64; c += 16) {
-        float u[16];
-        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_U + 64 * hf + c), u);
-        sm100::tmem_wait_ld();
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          dst[(c / 4 + q4) * 64 + r] =
-              make_float4(u[4 * q4], u[4 * q4 + 1], u[4 * q4 + 2], u[4 * q4 + 3]);
-      }
-    }
     SPLIT_MARK(10, mk);
 #ifdef KDA_PHASE_TIMING
     if (mk) atomicAdd(&kda_split_cycles[12], 1ull);  // items measured
@@ -630,7 +629,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   // before the shared and tensor memory are released (at most one copy per
   // barrier is outstanding)
   if (*s_abort) {
-    if (qg_issued > qg_done) sm100::mbar_wait(bar_qg, qg_done & 1, 200000000ull);
+    if (q_issued > q_done) sm100::mbar_wait(bar_q, q_done & 1, 200000000ull);
+    if (g_issued > g_done) sm100::mbar_wait(bar_g, g_done & 1, 200000000ull);
     if (k_issued > k_done) sm100::mbar_wait(bar_k, k_done & 1, 200000000ull);
     if (v_issued > v_done) sm100::mbar_wait(bar_v, v_done & 1, 200000000ull);
     if (mma_pending) sm100::mbar_wait(bar_mma, mma_phase & 1, 200000000ull);
@@ -653,6 +653,7 @@ static_assert(S_SMEM <= 232448, "shared memory");
 constexpr uint32_t S_TM_COLS = 256;
 constexpr uint32_t TM_S = 0;    // state half: 128 lanes (key channel) x 64 columns
 constexpr uint32_t TM_P = 64;   // two buffers of [W S; Q gamma S (+ A_qk Delta)], 64 columns each
+constexpr uint32_t TM_U = 192;  // U = T (beta V) of the half (lanes 0..63 = rows)
 
 __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitParams sp) {
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -678,8 +679,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
     const unsigned char* src = rec0 + (int64_t)c * REC_BYTES;
     uint64_t* bar = bar_full + (c & 1);
     sm100::mbar_arrive_expect_tx(bar, STAGE_BYTES);
-    sm100::bulk_load(st + ST_KD, src + REC_KD, REC_U - REC_KD, bar);
-    sm100::bulk_load(st + ST_U, src + REC_U + half * 16384, 16384, bar);
+    sm100::bulk_load(st + ST_KD, src + REC_KD, REC_BV - REC_KD, bar);
+    sm100::bulk_load(st + ST_BV, src + REC_BV + half * 8192, 8192, bar);
     sm100::bulk_load(st + ST_GC, src + REC_GC, 512, bar);
   };
 
@@ -717,6 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
 
   uint32_t mma_phase = 0;
   bool mma_pending = false;
+  bool u_open = false;           // thread 0: a U product not yet followed by a commit
   int issued = nc < 2 ? nc : 2;  // chunks whose record copy has been issued
   int landed = 0;                 // chunks whose record copy has been waited for
   // one thread waits for the products; the others meet it at the barrier
@@ -770,10 +772,23 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
     const int s = c & 1;
     const unsigned char* st = smem + s * STAGE_BYTES;
     const uint32_t tm_p = TM_P + 64 * s;
-    if (!sm100::mbar_wait(bar_full + s, (uint32_t)((c >> 1) & 1)))
+    if (!sm100::mbar_wait(bar_full + s, (uint32_t)((c >> 1) & 1))) {
       record_error(p, s_abort, KDA_ERR_TIMEOUT);
-    else
+    } else {
       landed = c + 1;
+      // U = [T; -] (beta V) of this half, while the CUDA cores copy S (the
+      // P product's commit covers it)
+      if (tid == 0) {
+        const uint32_t idu = sm100::idesc_bf16(128, 64, 0, 0);
+        const uint32_t s_t = sm100::smem_u32(st + ST_T);
+        const uint32_t s_bv = sm100::smem_u32(st + ST_BV);
+#pragma unroll
+        for (int k = 0; k < C / 16; ++k)
+          sm100::mma_ss(tmem + TM_U, sm100::smem_desc(s_t + 256 * k, 128, 1024),
+                        sm100::smem_desc(s_bv + 256 * k, 128, 1024), idu, k > 0);
+        u_open = true;
+      }
+    }
     SPLIT_MARK(17, mk);
 
     // (1) bf16 copy of S (B of the P product) and S <- gamma_C S ahead of the
@@ -817,6 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
         sm100::mma_ss(tmem + tm_p, sm100::smem_desc(sa + k * 4096, 2048, 128),
                       sm100::smem_desc(sb + k * 2048, 1024, 128), idesc, k > 0);
       sm100::mma_commit(bar_mma);
+      u_open = false;
     }
     mma_pending = true;
     // output rows of the previous chunk while the tensor cores work on P
@@ -830,20 +846,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
       float d[32];
 #pragma unroll
       for (int c16 = 0; c16 < 32; c16 += 16) {
-        float v[16];
+        float v[16], u[16];
         sm100::tmem_ld16(sm100::taddr(tmem, lane_q, tm_p + cb + c16), v);
+        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_U + cb + c16), u);
+        sm100::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) d[c16 + e] = v[e];
-      }
-      sm100::tmem_wait_ld();
-      const float4* u4 = reinterpret_cast<const float4*>(st + ST_U);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 u = u4[(cb / 4 + q) * 64 + r];
-        d[4 * q] = u.x - d[4 * q];
-        d[4 * q + 1] = u.y - d[4 * q + 1];
-        d[4 * q + 2] = u.z - d[4 * q + 2];
-        d[4 * q + 3] = u.w - d[4 * q + 3];
+        for (int e = 0; e < 16; ++e) d[c16 + e] = u[e] - v[e];
       }
 #pragma unroll
       for (int g = 0; g < 4; ++g)
@@ -909,7 +917,12 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
   }
 
   if (*s_abort) {
-    // bounded waits for copies and products still in flight
+    // bounded waits for copies and products still in flight (a U product
+    // that no commit follows gets one first)
+    if (tid == 0 && u_open) {
+      sm100::mma_commit(bar_mma);
+      mma_pending = true;
+    }
     if (mma_pending) sm100::mbar_wait(bar_mma, mma_phase & 1, 200000000ull);
     for (int k = landed; k < issued; ++k)
       sm100::mbar_wait(bar_full + (k & 1), (uint32_t)((k >> 1) & 1), 200000000ull);

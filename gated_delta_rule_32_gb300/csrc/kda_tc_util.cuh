@@ -113,10 +113,12 @@ __device__ __forceinline__ void store_tile(const float (&d)[4], float* D, int ld
 // from `a` (row stride LD floats; blocks above the block diagonal are never
 // read), the strictly lower part of T is left in `tf` (same stride), `y`
 // ([32][36] fp32) is scratch, and T itself (unit diagonal, zero above) is
-// written as bf16 K-major [r][i] to `t_bf16`.
+// written as bf16 K-major [r][i] to `t_bf16` (shared memory) and, when
+// `t_copy` is not null, to `t_copy` too (global memory, same layout).
 template <int LD>
 __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, float* y,
-                                                   unsigned char* t_bf16, int tid) {
+                                                   unsigned char* t_bf16, int tid,
+                                                   unsigned char* t_copy = nullptr) {
   const int warp = tid >> 5, lane = tid & 31;
   {
     const int blk = warp >> 1, c = (warp & 1) * 8 + (lane >> 2), q = lane & 3;
@@ -192,6 +194,7 @@ __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, fl
       t[c] = (i < r) ? tf[r * LD + i] : (i == r ? 1.0f : 0.0f);
     }
     st8_bf16(t_bf16 + k64_off(r, i0), t);
+    if (t_copy) st8_bf16(t_copy + k64_off(r, i0), t);
   }
 }
 

@@ -122,7 +122,7 @@ kda_status kda_chunk_fwd_f32(const float* q, const float* k, const float* v,
  *               allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
  *               256-byte aligned.  The two-kernel path (KDA_ALGO_SPLIT)
  *               also accepts less, down to one chunk record per (sequence,
- *               head) plus the carried state (N * H * (90624 + 65536)
+ *               head) plus the carried state (N * H * (82432 + 65536)
  *               bytes, rounded up to 256): it then runs the sequence in
  *               more, shorter slices; below that KDA_ERR_WORKSPACE.
  *   dev_status  NULL or one device int32; set to KDA_OK at the start of the

@@ -100,12 +100,12 @@ def test_package_fails_loudly_without_library(tmp_path):
 
 def test_split_path_host_checks(lib):
     # workspace sizing of the two-kernel path: carried state + one slice of
-    # 90624-byte chunk records per (sequence, head); packed batches need none
+    # 82432-byte chunk records per (sequence, head); packed batches need none
     carry = 2 * 32 * 128 * 128 * 4
     nb = kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=kda.KDA_ALGO_SPLIT)
-    assert nb == carry + 2 * 32 * 512 * 90624
+    assert nb == carry + 2 * 32 * 512 * 82432
     assert kda.kda_workspace_bytes(2, 100, 1, 128, 128, algo=kda.KDA_ALGO_SPLIT) == \
-        2 * 128 * 128 * 4 + 2 * 2 * 90624
+        2 * 128 * 128 * 4 + 2 * 2 * 82432
     assert kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=kda.KDA_ALGO_SPLIT,
                                    packed=1) == 0
     assert kda.kda_resolve_algo(kda.KDA_BF16, 128, 128, 0, kda.KDA_ALGO_SPLIT) == \

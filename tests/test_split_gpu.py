@@ -19,7 +19,7 @@ from kda_inputs import WORKLOADS, make_inputs, make_unit, small_workload
 pytestmark = pytest.mark.gpu
 
 SPLIT = kda.KDA_ALGO_SPLIT
-REC = 90624  # bytes of one chunk record
+REC = 82432  # bytes of one chunk record
 
 
 @pytest.fixture(scope="module", autouse=True)
