@@ -567,13 +567,17 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ---- T = (I + beta A_kk)^{-1} -------------------------------------------
     unit_lower_inverse<AKK_LD>(s_akk, reinterpret_cast<float*>(smem + I_TF),
-                               reinterpret_cast<float*>(smem + I_Y), smem + I_T, tid,
-                               rec + REC_T);
+                               reinterpret_cast<float*>(smem + I_Y), smem + I_T, tid);
     sm100::fence_async_smem();
     sync_all();
     SPLIT_MARK(8, mk);
-    // the solve scratch (over V's landing zone) and beta are dead: the next
-    // item's V tiles and beta
+    // T into the record by one bulk copy (read out of shared memory before
+    // the next item's Q lands there); the solve scratch (over V's landing
+    // zone) and beta are dead: the next item's V tiles and beta
+    if (tid == 32) {
+      sm100::bulk_store(rec + REC_T, smem + I_T, 8192);
+      sm100::bulk_commit();
+    }
     if (has_next) {
       if (tid == 32) load_v(nxt);
       v_issued = li + 2;
@@ -596,9 +600,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     wait_mma();
     SPLIT_MARK(9, mk);
     if (*s_abort) break;
-    // T (over Q) is dead: the next item's Q tiles
+    // T (over Q) is dead once its copy to the record has read it: the next
+    // item's Q tiles
     if (has_next) {
-      if (tid == 32) load_q(nxt);
+      if (tid == 32) {
+        sm100::bulk_wait_read();
+        load_q(nxt);
+      }
       q_issued = li + 2;
     }
 
@@ -635,6 +643,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (v_issued > v_done) sm100::mbar_wait(bar_v, v_done & 1, 200000000ull);
     if (mma_pending) sm100::mbar_wait(bar_mma, mma_phase & 1, 200000000ull);
   }
+  if (tid == 32) sm100::bulk_wait();  // the last T copy
   sm100::tc_fence_before();
   __syncthreads();
   if (warp == 0) sm100::tmem_dealloc(tmem, I_TM_COLS);

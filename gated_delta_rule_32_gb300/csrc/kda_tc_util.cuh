@@ -72,12 +72,16 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 // D(16x8 tile) += A[a_row0.., a_col0 + k..] * B[b_row0 + k.., b_col0..] over
-// k in [k0, k1) (multiples of 8); A, B fp32 row-major with leading dims.
+// k in [K0, K1) (multiples of 8, fixed at compile time so that every
+// fragment load is issued ahead of the products); A, B fp32 row-major with
+// leading dims.
+template <int K0, int K1>
 __device__ __forceinline__ void mma_tile(float (&d)[4], const float* A, int lda, int a_row0,
                                          int a_col0, const float* B, int ldb, int b_row0,
-                                         int b_col0, int k0, int k1, int lane) {
+                                         int b_col0, int lane) {
   const int g = lane >> 2, t = lane & 3;
-  for (int k = k0; k < k1; k += 8) {
+#pragma unroll
+  for (int k = K0; k < K1; k += 8) {
     uint32_t a[4], b[2];
     const float* Ar = A + (a_row0 + g) * lda + a_col0 + k + t;
     a[0] = tf32_of(Ar[0]);
@@ -113,12 +117,12 @@ __device__ __forceinline__ void store_tile(const float (&d)[4], float* D, int ld
 // from `a` (row stride LD floats; blocks above the block diagonal are never
 // read), the strictly lower part of T is left in `tf` (same stride), `y`
 // ([32][36] fp32) is scratch, and T itself (unit diagonal, zero above) is
-// written as bf16 K-major [r][i] to `t_bf16` (shared memory) and, when
-// `t_copy` is not null, to `t_copy` too (global memory, same layout).
+// written as bf16 K-major [r][i] to `t_bf16`.  LD is a multiple of 4 (rows
+// are read as float4).
 template <int LD>
 __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, float* y,
-                                                   unsigned char* t_bf16, int tid,
-                                                   unsigned char* t_copy = nullptr) {
+                                                   unsigned char* t_bf16, int tid) {
+  static_assert(LD % 4 == 0, "row stride");
   const int warp = tid >> 5, lane = tid & 31;
   {
     const int blk = warp >> 1, c = (warp & 1) * 8 + (lane >> 2), q = lane & 3;
@@ -155,7 +159,7 @@ __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, fl
     const int hh = warp >> 1, nt = (warp & 1) * 8;
     const int a1 = 2 * hh + 1, a0 = 2 * hh;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_tile(d, a, LD, 16 * a1, 16 * a0, tf, LD, 16 * a0, 16 * a0 + nt, 0, 16, lane);
+    mma_tile<0, 16>(d, a, LD, 16 * a1, 16 * a0, tf, LD, 16 * a0, 16 * a0 + nt, lane);
     store_tile(d, y, 36, 16 * hh, nt, 1.0f, lane);
   }
   __syncthreads();
@@ -163,7 +167,7 @@ __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, fl
     const int hh = warp >> 1, nt = (warp & 1) * 8;
     const int a1 = 2 * hh + 1, a0 = 2 * hh;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_tile(d, tf, LD, 16 * a1, 16 * a1, y, 36, 16 * hh, nt, 0, 16, lane);
+    mma_tile<0, 16>(d, tf, LD, 16 * a1, 16 * a1, y, 36, 16 * hh, nt, lane);
     store_tile(d, tf, LD, 16 * a1, 16 * a0 + nt, -1.0f, lane);
   }
   __syncthreads();
@@ -171,8 +175,14 @@ __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, fl
   {
     const int mt = (warp >> 2) * 16, nt = (warp & 3) * 8;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
-    // Y = A[H1, H0] T[H0, H0] (T lower triangular: k from the tile's column)
-    mma_tile(d, a, LD, 32 + mt, 0, tf, LD, 0, nt, nt & ~7, 32, lane);
+    // Y = A[H1, H0] T[H0, H0] (T lower triangular: k from the tile's column;
+    // the block above T's diagonal tiles is never written, so it is skipped)
+    switch (nt >> 3) {
+      case 0: mma_tile<0, 32>(d, a, LD, 32 + mt, 0, tf, LD, 0, nt, lane); break;
+      case 1: mma_tile<8, 32>(d, a, LD, 32 + mt, 0, tf, LD, 0, nt, lane); break;
+      case 2: mma_tile<16, 32>(d, a, LD, 32 + mt, 0, tf, LD, 0, nt, lane); break;
+      default: mma_tile<24, 32>(d, a, LD, 32 + mt, 0, tf, LD, 0, nt, lane); break;
+    }
     store_tile(d, y, 36, mt, nt, 1.0f, lane);
   }
   __syncthreads();
@@ -180,21 +190,28 @@ __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, fl
     const int mt = (warp >> 2) * 16, nt = (warp & 3) * 8;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     // T[H1, H0] = -T[H1, H1] Y (T[H1, H1] lower triangular: k up to the row tile)
-    mma_tile(d, tf, LD, 32 + mt, 32, y, 36, 0, nt, 0, mt + 16, lane);
+    if (mt == 0) mma_tile<0, 16>(d, tf, LD, 32, 32, y, 36, 0, nt, lane);
+    else mma_tile<0, 32>(d, tf, LD, 48, 32, y, 36, 0, nt, lane);
     store_tile(d, tf, LD, 32 + mt, nt, -1.0f, lane);
   }
   __syncthreads();
   // T as bf16, K-major [r][i], unit diagonal, zero above
-  for (int e = tid; e < 512; e += 256) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int e = tid + 256 * h;
     const int r = e >> 3, i0 = (e & 7) * 8;
+    // the whole 8-wide row piece, entries on and above the diagonal then
+    // replaced (they may never have been written)
+    const float4 v0 = *reinterpret_cast<const float4*>(tf + r * LD + i0);
+    const float4 v1 = *reinterpret_cast<const float4*>(tf + r * LD + i0 + 4);
+    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     float t[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const int i = i0 + c;
-      t[c] = (i < r) ? tf[r * LD + i] : (i == r ? 1.0f : 0.0f);
+      t[c] = (i < r) ? v[c] : (i == r ? 1.0f : 0.0f);
     }
     st8_bf16(t_bf16 + k64_off(r, i0), t);
-    if (t_copy) st8_bf16(t_copy + k64_off(r, i0), t);
   }
 }
 

@@ -93,6 +93,25 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Untiled bulk copy shared -> global of `bytes` bytes (both addresses 16-byte
+// aligned, a multiple of 16 bytes), tracked by the issuing thread's bulk
+// async-group; then the group commit and the waits: until the source may be
+// overwritten (`bulk_wait_read`), until the writes are done (`bulk_wait`).
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               ::"l"(reinterpret_cast<uint64_t>(dst)), "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // proxy / tcgen05 ordering fences
 __device__ __forceinline__ void fence_async_smem() {
