@@ -101,6 +101,7 @@ constexpr int I_B2 = I_OB + 32768;                 // c0'               MN-major
 constexpr int I_BKG = I_OB + 36864;                // (beta K gamma)^T K-major 128 x 64
 constexpr int I_BETA = I_BKG + 16384;              // 64 raw bf16
 constexpr int I_PT = I_BETA + 128;                 // [4 tiles][128] fp32 tile products
+static_assert(I_BETA % 16 == 0, "beta rows are read 8 at a time");
 constexpr int I_BAR = I_PT + 2048;
 constexpr int I_MISC = I_BAR + 64;
 constexpr int I_SMEM = I_MISC + 64;
@@ -316,17 +317,28 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!sm100::mbar_wait(bar_v, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
     else v_done = li + 1;
     {
-      const int jv = tid & 127, rh = tid >> 7;
+      // thread: value channels jv, jv + 1 (one bf16 pair per row) of rows
+      // 16 rq .. 16 rq + 15; beta of those rows in two 16-byte loads
+      const int jv = 2 * (tid & 63), rq = tid >> 6, cl = jv & 63;
       const unsigned char* sv = smem + I_V + (jv >> 6) * 8192;
+      const uint4 bq0 = *reinterpret_cast<const uint4*>(smem + I_BETA + 32 * rq);
+      const uint4 bq1 = *reinterpret_cast<const uint4*>(smem + I_BETA + 32 * rq + 16);
+      const uint32_t bw[8] = {bq0.x, bq0.y, bq0.z, bq0.w, bq1.x, bq1.y, bq1.z, bq1.w};
+      float t0[16], t1[16];
 #pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        float t[8];
+      for (int e = 0; e < 16; ++e) {
+        const int r = 16 * rq + e;
+        const uint32_t vv = *reinterpret_cast<const uint32_t*>(sv + sw128_off(r, cl));
+        const uint32_t bb = bw[e >> 1];
+        const float b = __uint_as_float((e & 1) ? (bb & 0xFFFF0000u) : (bb << 16));
+        const bool in = r < L;
+        t0[e] = in ? b * __uint_as_float(vv << 16) : 0.0f;
+        t1[e] = in ? b * __uint_as_float(vv & 0xFFFF0000u) : 0.0f;
+      }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int r = 32 * rh + 8 * g8 + e;
-          t[e] = (r < L) ? beta_at(r) * ld_bf16(sv, sw128_off(r, jv & 63)) : 0.0f;
-        }
-        st8_bf16(rec + REC_BV + k64_off(jv, 32 * rh + 8 * g8), t);
+      for (int hh = 0; hh < 2; ++hh) {
+        st8_bf16(rec + REC_BV + k64_off(jv, 16 * rq + 8 * hh), t0 + 8 * hh);
+        st8_bf16(rec + REC_BV + k64_off(jv + 1, 16 * rq + 8 * hh), t1 + 8 * hh);
       }
     }
     __syncthreads();
@@ -416,9 +428,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int i = 0; i < 8; ++i) t[i] = qE[i] * preq;
         st8_bf16(rec + REC_WQ + mn_off(64 + r0, j, 2048), t);
-        // (beta K gamma)^T, K-major [j][r]
+        // (beta K gamma)^T, K-major [j][r] (beta of the 8 rows: one 16-byte load)
+        {
+          const uint4 bq = *reinterpret_cast<const uint4*>(smem + I_BETA + 2 * r0);
+          const uint32_t bw[4] = {bq.x, bq.y, bq.z, bq.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = beta_at(r0 + i) * kE[i] * pre;
+          for (int i = 0; i < 8; ++i)
+            t[i] = __uint_as_float((i & 1) ? (bw[i >> 1] & 0xFFFF0000u) : (bw[i >> 1] << 16)) *
+                   kE[i] * pre;
+        }
         st8_bf16(smem + I_BKG + k64_off(j, r0), t);
         // (K e^{G_C - G})^T, K-major [j][r]
 #pragma unroll
