@@ -69,8 +69,10 @@ constexpr int AKK_LD = 72;                        // fp32 row stride (floats)
 constexpr int OFF_AKK = OFF_R1;                   // [64][72] fp32   18432
 constexpr int OFF_TF = OFF_AKK + 18432;           // [64][72] fp32   18432
 constexpr int OFF_T = OFF_TF + 18432;             // T bf16 K-major   8192
-// [32][36] fp32 products of the block merges (4608 B), dead before T is written
-constexpr int OFF_Y = OFF_T;
+// [32][36] fp32 products of the block merges (4608 B), in the landing zone:
+// the chunk's tiles have been read for the last time before the solve and
+// the next chunk's are requested after it
+constexpr int OFF_Y = OFF_Q;
 
 // The rest of the map depends on the kernel mode: MODE 0 is the forward
 // (state half: 64 value columns); MODE 1 is the segment summary, which

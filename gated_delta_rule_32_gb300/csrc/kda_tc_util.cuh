@@ -104,6 +104,17 @@ __device__ __forceinline__ void store_tile(const float (&d)[4], float* D, int ld
   *reinterpret_cast<float2*>(r1) = make_float2(sc * d[2], sc * d[3]);
 }
 
+// bf16 copy of a 16x8 accumulator tile (scaled) into a K-major [r][i]
+// operand with K extent 64 (one packed pair per row and lane)
+__device__ __forceinline__ void store_tile_bf16(const float (&d)[4], unsigned char* t, int row0,
+                                                int col0, float sc, int lane) {
+  const int g = lane >> 2, c0 = col0 + 2 * (lane & 3);
+  *reinterpret_cast<uint32_t*>(t + k64_off(row0 + g, c0)) =
+      sm100::pack_bf16x2(sc * d[0], sc * d[1]);
+  *reinterpret_cast<uint32_t*>(t + k64_off(row0 + g + 8, c0)) =
+      sm100::pack_bf16x2(sc * d[2], sc * d[3]);
+}
+
 // ---------------------------------------------------------------------------
 // T = (I + A)^{-1} for a strictly lower triangular 64 x 64 fp32 matrix A
 // (A = diag(beta) A_kk of one chunk), blocked by 16 x 16 tiles:
@@ -111,14 +122,18 @@ __device__ __forceinline__ void store_tile(const float (&d)[4], float* D, int ld
 //     lanes, right-looking substitution in registers (critical path: 15
 //     FMAs), lane q of a group owning rows q, q+4, q+8, q+12 and the pivot
 //     arriving by shuffle;
-// (2) T[2h+1, 2h] = -T[2h+1, 2h+1] A[2h+1, 2h] T[2h, 2h] for h = 0, 1;
+// (2) T[2h+1, 2h] = -T[2h+1, 2h+1] (A[2h+1, 2h] T[2h, 2h]) for h = 0, 1, one
+//     16 x 8 column tile per warp (warps 0-3), the inner product kept in
+//     registers and turned into the outer product's operand by shuffles;
+//     warps 4-7 meanwhile zero the tiles of T above the block diagonal;
 // (3) T[H1, H0]  = -T[H1, H1] A[H1, H0] T[H0, H0] on the 32 x 32 halves.
-// Called by all 256 threads of the CTA (it synchronises them).  A is read
-// from `a` (row stride LD floats; blocks above the block diagonal are never
-// read), the strictly lower part of T is left in `tf` (same stride), `y`
-// ([32][36] fp32) is scratch, and T itself (unit diagonal, zero above) is
-// written as bf16 K-major [r][i] to `t_bf16`.  LD is a multiple of 4 (rows
-// are read as float4).
+// Each tile of T is written as bf16 by the step that makes it.
+// Called by all 256 threads of the CTA (it synchronises them, but not after
+// the last step).  A is read from `a` (row stride LD floats; blocks above
+// the block diagonal are never read), the strictly lower part of T is left
+// in `tf` (same stride), `y` ([32][36] fp32) is scratch, and T itself (unit
+// diagonal, zero above) is written as bf16 K-major [r][i] to `t_bf16`.
+// LD is a multiple of 4 (rows are read as float4).
 template <int LD>
 __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, float* y,
                                                    unsigned char* t_bf16, int tid) {
@@ -150,25 +165,57 @@ __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, fl
       }
     }
 #pragma unroll
-    for (int k4 = 0; k4 < 4; ++k4) tf[(16 * blk + 4 * k4 + q) * LD + 16 * blk + c] = x[k4];
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const int r = 16 * blk + 4 * k4 + q;
+      tf[r * LD + 16 * blk + c] = x[k4];
+      *reinterpret_cast<__nv_bfloat16*>(t_bf16 + k64_off(r, 16 * blk + c)) =
+          __float2bfloat16_rn(x[k4]);
+    }
   }
   __syncthreads();
-  // (2) Y_h = A[2h+1, 2h] T[2h, 2h], T[2h+1, 2h] = -T[2h+1, 2h+1] Y_h;
-  //     warp w < 4: h = w >> 1, 8-column tile w & 1
   if (warp < 4) {
+    // (2) warp w: h = w >> 1, 8-column tile w & 1
     const int hh = warp >> 1, nt = (warp & 1) * 8;
     const int a1 = 2 * hh + 1, a0 = 2 * hh;
+    const int g = lane >> 2, t = lane & 3;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
+    // Y = A[2h+1, 2h] T[2h, 2h] (16 x 8 tile, accumulator layout)
     mma_tile<0, 16>(d, a, LD, 16 * a1, 16 * a0, tf, LD, 16 * a0, 16 * a0 + nt, lane);
-    store_tile(d, y, 36, 16 * hh, nt, 1.0f, lane);
-  }
-  __syncthreads();
-  if (warp < 4) {
-    const int hh = warp >> 1, nt = (warp & 1) * 8;
-    const int a1 = 2 * hh + 1, a0 = 2 * hh;
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_tile<0, 16>(d, tf, LD, 16 * a1, 16 * a1, y, 36, 16 * hh, nt, lane);
-    store_tile(d, tf, LD, 16 * a1, 16 * a0 + nt, -1.0f, lane);
+    // operand fragments of Y for the second product: lane (g, t) takes
+    // Y[t + 4u][g] (u = 0..3), held by lane 4 (t + 4u mod 8) + g / 2 as its
+    // element 2 (u / 2) + g % 2
+    const int s0 = 4 * t + (g >> 1), s1 = s0 + 16;
+    float y0[4], y1[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      y0[e] = __shfl_sync(0xffffffffu, d[e], s0);
+      y1[e] = __shfl_sync(0xffffffffu, d[e], s1);
+    }
+    const bool odd = (g & 1) != 0;
+    const uint32_t bk0[2] = {tf32_of(odd ? y0[1] : y0[0]), tf32_of(odd ? y1[1] : y1[0])};
+    const uint32_t bk1[2] = {tf32_of(odd ? y0[3] : y0[2]), tf32_of(odd ? y1[3] : y1[2])};
+    // T[2h+1, 2h] = -T[2h+1, 2h+1] Y
+    float e2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      const float* Ar = tf + (16 * a1 + g) * LD + 16 * a1 + 8 * ks + t;
+      const uint32_t af[4] = {tf32_of(Ar[0]), tf32_of(Ar[8 * LD]), tf32_of(Ar[4]),
+                              tf32_of(Ar[8 * LD + 4])};
+      mma_tf32(e2, af, ks ? bk1 : bk0);
+    }
+    store_tile(e2, tf, LD, 16 * a1, 16 * a0 + nt, -1.0f, lane);
+    store_tile_bf16(e2, t_bf16, 16 * a1, 16 * a0 + nt, -1.0f, lane);
+  } else {
+    // zero the six 16 x 16 tiles above the block diagonal: 24 core matrices
+    // of 128 bytes, written 16 bytes at a time
+    for (int e = tid - 128; e < 24 * 8; e += 128) {
+      const int cm = e >> 3, piece = e & 7, tix = cm >> 2, sub = cm & 3;
+      const int R = tix < 3 ? 0 : (tix < 5 ? 1 : 2);
+      const int I = tix < 3 ? tix + 1 : (tix < 5 ? tix - 1 : 3);
+      *reinterpret_cast<uint4*>(t_bf16 + (2 * R + (sub >> 1)) * 1024 +
+                                (2 * I + (sub & 1)) * 128 + piece * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
   }
   __syncthreads();
   // (3) level 2 on the 32 x 32 halves; warp w: rows 16 (w >> 2), columns 8 (w & 3)
@@ -193,25 +240,7 @@ __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, fl
     if (mt == 0) mma_tile<0, 16>(d, tf, LD, 32, 32, y, 36, 0, nt, lane);
     else mma_tile<0, 32>(d, tf, LD, 48, 32, y, 36, 0, nt, lane);
     store_tile(d, tf, LD, 32 + mt, nt, -1.0f, lane);
-  }
-  __syncthreads();
-  // T as bf16, K-major [r][i], unit diagonal, zero above
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int e = tid + 256 * h;
-    const int r = e >> 3, i0 = (e & 7) * 8;
-    // the whole 8-wide row piece, entries on and above the diagonal then
-    // replaced (they may never have been written)
-    const float4 v0 = *reinterpret_cast<const float4*>(tf + r * LD + i0);
-    const float4 v1 = *reinterpret_cast<const float4*>(tf + r * LD + i0 + 4);
-    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float t[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int i = i0 + c;
-      t[c] = (i < r) ? v[c] : (i == r ? 1.0f : 0.0f);
-    }
-    st8_bf16(t_bf16 + k64_off(r, i0), t);
+    store_tile_bf16(d, t_bf16, 32 + mt, nt, -1.0f, lane);
   }
 }
 
