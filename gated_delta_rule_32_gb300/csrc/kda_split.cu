@@ -271,6 +271,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (!sm100::mbar_wait(bar_g, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
     else g_done = li + 1;
     if (tid < C) s_beta_raw[tid] = beta_raw;  // bf16 bits; readers widen them
+    // the next item's beta, a whole item ahead of its use
+    if (has_next) beta_raw = load_beta(nxt);
     // rows past the end of the sequence (its last chunk only): a decay logit
     // far below zero (alpha = 1), so that no later step masks
     if (L < C) {
@@ -591,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     SPLIT_MARK(8, mk);
     // T into the record by one bulk copy (read out of shared memory before
     // the next item's Q lands there); the solve scratch (over V's landing
-    // zone) and beta are dead: the next item's V tiles and beta
+    // zone) is dead: the next item's V tiles
     if (tid == 32) {
       sm100::bulk_store(rec + REC_T, smem + I_T, 8192);
       sm100::bulk_commit();
@@ -599,7 +601,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (has_next) {
       if (tid == 32) load_v(nxt);
       v_issued = li + 2;
-      beta_raw = load_beta(nxt);
     }
 
     // ---- W^T = (beta K gamma)^T T^T (U = T (beta V) is formed by the state
