@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int s = 0; s < 16; ++s) {
         const int r = 16 * a + s;
-        const uint32_t o = sw128_off(r, jl);
+        const uint32_t o = row_off(r, jl);
         al0[s] = alpha_of(ld_bf16(g0, o));
         al1[s] = alpha_of(ld_bf16(g1, o));
         p0 *= al0[s];
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
         const int r = 16 * rq + e;
-        const uint32_t vv = *reinterpret_cast<const uint32_t*>(sv + sw128_off(r, cl));
+        const uint32_t vv = *reinterpret_cast<const uint32_t*>(sv + row_off(r, cl));
         const uint32_t bb = bw[e >> 1];
         const float b = __uint_as_float((e & 1) ? (bb & 0xFFFF0000u) : (bb << 16));
         const bool in = r < L;
@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int e8 = 0; e8 < 8; ++e8) {
           const int r = r0 + e8;
-          const uint32_t o = sw128_off(r, jl);
+          const uint32_t o = row_off(r, jl);
           const float qv = ld_bf16(sq, o);
           const float kv = ld_bf16(sk, o);
           e *= al[8 * g + e8];
@@ -1037,8 +1037,9 @@ kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_
   const int slice = fit < (size_t)nchunks ? (int)fit : nchunks;
   if (one_slice && slice < nchunks) return KDA_ERR_WORKSPACE;
   CUtensorMap mq, mk, mg, mv;
-  if (!make_map(&mq, p.q, rows, p.H, DK) || !make_map(&mk, p.k, rows, p.H, DK) ||
-      !make_map(&mg, p.g, rows, p.H, DK) || !make_map(&mv, p.v, rows, p.H, DV))
+  // unswizzled tiles: every read of them goes along one row
+  if (!make_map(&mq, p.q, rows, p.H, DK, false) || !make_map(&mk, p.k, rows, p.H, DK, false) ||
+      !make_map(&mg, p.g, rows, p.H, DK, false) || !make_map(&mv, p.v, rows, p.H, DV, false))
     return KDA_ERR_CUDA;
   static bool attr_set = false;
   if (!attr_set) {

@@ -26,6 +26,11 @@ __device__ __forceinline__ uint32_t k64_off(int mn, int k) {
 __device__ __forceinline__ uint32_t sw128_off(int row, int ch) {
   return (uint32_t)row * 128u + (uint32_t)(((ch >> 3) ^ (row & 7)) << 4) + (uint32_t)(ch & 7) * 2u;
 }
+// unswizzled TMA row: element (row, ch) of a [rows][64] bf16 box (conflict-free
+// as long as a warp reads along one row)
+__device__ __forceinline__ uint32_t row_off(int row, int ch) {
+  return (uint32_t)row * 128u + (uint32_t)ch * 2u;
+}
 __device__ __forceinline__ float ld_bf16(const unsigned char* base, uint32_t off) {
   return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + off));
 }
@@ -259,8 +264,10 @@ inline PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 3-D map over a [rows, H, d] bf16 tensor: box = 64 channels x 1 head x 64 rows
-inline bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H, int d) {
+// 3-D map over a [rows, H, d] bf16 tensor: box = 64 channels x 1 head x 64 rows,
+// rows 128B-swizzled in shared memory unless `swizzle` is false
+inline bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H, int d,
+                     bool swizzle = true) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
@@ -268,7 +275,8 @@ inline bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H, int 
   cuuint32_t box[3] = {64, 1, 64};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
