@@ -109,6 +109,27 @@ kda_status kda_run_split(const kda::FwdParams& p, void* workspace, size_t worksp
                          cudaStream_t stream);
 size_t kda_split_workspace_bytes(int N, int T, int H);
 size_t kda_split_min_workspace_bytes(int N, int H);
+kda_status kda_run_split_range(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream, int c0, int cnt);
+size_t kda_split_slice_workspace_bytes(int N, int H, int chunks);
+
+namespace {
+// The end-to-end call on the two-kernel path runs the sequence in pieces of
+// whole chunks: the inputs of piece i + 1 go to the device on two copy
+// streams while piece i runs on the caller's stream and the output of piece
+// i - 1 comes back on a third, so the host link, not the sum of copies and
+// kernels, sets the time.  The state crosses pieces exactly as it crosses
+// slices (fp32, unchanged), so the result does not depend on the cut.
+constexpr int kHostPieces = 8;
+int host_piece_chunks(int T) {
+  const int nchunks = (T + 63) / 64;
+  const int pieces = nchunks < kHostPieces ? nchunks : kHostPieces;
+  return (nchunks + pieces - 1) / pieces;
+}
+bool host_pipelined(int dtype, int dk, int dv, int packed, int T) {
+  return use_split(dtype, dk, dv, 0, KDA_ALGO_AUTO, packed, T) && (T + 63) / 64 >= 2;
+}
+}  // namespace
 // A workspace smaller than the default (but at least the minimum) runs the
 // sequence in more, shorter slices.
 static kda_status run_split_ws(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
@@ -314,11 +335,111 @@ size_t kda_host_staging_bytes(int B, int T, int H, int dk, int dv, int dtype, in
   if (has_init) tot += round_up(s.state);
   if (has_final) tot += round_up(s.state);
   tot += round_up(s.cu) + 256;  // cu_seqlens + device status word
-  // the path's own workspace (chunk records of the two-kernel form, or the
-  // segment scratch), so that the end-to-end call allocates nothing itself
-  tot += round_up(kda_workspace_bytes(B, T, H, dk, dv, dtype, 0, KDA_ALGO_AUTO, packed));
+  // the path's own workspace (chunk records of one piece of the two-kernel
+  // form, or the segment scratch), so that the end-to-end call allocates
+  // nothing itself
+  if (host_pipelined(dtype, dk, dv, packed, T))
+    tot += round_up(kda_split_slice_workspace_bytes(B, H, host_piece_chunks(T)));
+  else
+    tot += round_up(kda_workspace_bytes(B, T, H, dk, dv, dtype, 0, KDA_ALGO_AUTO, packed));
   return tot;
 }
+
+}  // extern "C"
+
+namespace {
+// The pieces of a pipelined end-to-end call (see host_piece_chunks): bf16,
+// dk = dv = 128, dense.  Returns once everything is back on the host.
+kda_status host_pipelined_run(const void* q, const void* k, const void* v, const void* g_logit,
+                              const void* beta, const float* init_state, void* out,
+                              float* final_state, int B, int T, int H, float scale, char* dq,
+                              char* dk_, char* dv_, char* dg, char* db, float* ds0, char* dout,
+                              float* ds1, int32_t* dstat, void* ws, size_t ws_bytes,
+                              cudaStream_t stream) {
+  constexpr int D = 128;
+  const size_t row_qk = (size_t)H * D * 2, row_b = (size_t)H * 2;  // bytes per token row
+  const int nchunks = (T + 63) / 64, per = host_piece_chunks(T);
+  const int pieces = (nchunks + per - 1) / per;
+  cudaStream_t s_in[2] = {nullptr, nullptr}, s_out = nullptr;
+  cudaEvent_t ev0 = nullptr, ev_in[2][kHostPieces] = {}, ev_c[kHostPieces] = {};
+  kda_status st = KDA_OK;
+  auto cu = [&](cudaError_t e) {
+    if (e != cudaSuccess && st == KDA_OK) st = KDA_ERR_CUDA;
+    return st == KDA_OK;
+  };
+  cu(cudaStreamCreateWithFlags(&s_in[0], cudaStreamNonBlocking));
+  cu(cudaStreamCreateWithFlags(&s_in[1], cudaStreamNonBlocking));
+  cu(cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking));
+  cu(cudaEventCreateWithFlags(&ev0, cudaEventDisableTiming));
+  for (int i = 0; i < pieces; ++i) {
+    cu(cudaEventCreateWithFlags(&ev_in[0][i], cudaEventDisableTiming));
+    cu(cudaEventCreateWithFlags(&ev_in[1][i], cudaEventDisableTiming));
+    cu(cudaEventCreateWithFlags(&ev_c[i], cudaEventDisableTiming));
+  }
+  int32_t hstat = 0;
+  if (st == KDA_OK) {
+    kda::FwdParams p{};
+    p.q = dq; p.k = dk_; p.v = dv_; p.g = dg; p.beta = db;
+    p.init_state = ds0; p.out = dout; p.final_state = ds1; p.dev_status = dstat;
+    p.N = B; p.T = T; p.H = H; p.dk = D; p.dv = D; p.scale = scale;
+    // the copies start after whatever the caller queued on its stream
+    cu(cudaMemsetAsync(dstat, 0, sizeof(int32_t), stream));
+    cu(cudaEventRecord(ev0, stream));
+    cu(cudaStreamWaitEvent(s_in[0], ev0, 0));
+    cu(cudaStreamWaitEvent(s_in[1], ev0, 0));
+    auto h2d = [&](char* dst, const void* src, size_t off, size_t n, cudaStream_t sm) {
+      return cu(cudaMemcpyAsync(dst + off, static_cast<const char*>(src) + off, n,
+                                cudaMemcpyHostToDevice, sm));
+    };
+    for (int i = 0; i < pieces && st == KDA_OK; ++i) {
+      const int c0 = i * per, cnt = nchunks - c0 < per ? nchunks - c0 : per;
+      const size_t t0 = (size_t)c0 * 64;
+      const size_t t1 = (size_t)(c0 + cnt) * 64 < (size_t)T ? (size_t)(c0 + cnt) * 64 : (size_t)T;
+      for (int n = 0; n < B; ++n) {  // rows [t0, t1) of each sequence
+        const size_t r0 = (size_t)n * T + t0, nr = t1 - t0;
+        h2d(dq, q, r0 * row_qk, nr * row_qk, s_in[0]);
+        h2d(dk_, k, r0 * row_qk, nr * row_qk, s_in[0]);
+        h2d(dg, g_logit, r0 * row_qk, nr * row_qk, s_in[1]);
+        h2d(dv_, v, r0 * row_qk, nr * row_qk, s_in[1]);
+        h2d(db, beta, r0 * row_b, nr * row_b, s_in[1]);
+      }
+      if (i == 0 && ds0)
+        h2d(reinterpret_cast<char*>(ds0), init_state, 0, (size_t)B * H * D * D * 4, s_in[0]);
+      cu(cudaEventRecord(ev_in[0][i], s_in[0]));
+      cu(cudaEventRecord(ev_in[1][i], s_in[1]));
+      cu(cudaStreamWaitEvent(stream, ev_in[0][i], 0));
+      cu(cudaStreamWaitEvent(stream, ev_in[1][i], 0));
+      if (st == KDA_OK) st = kda_run_split_range(p, ws, ws_bytes, stream, c0, cnt);
+      cu(cudaEventRecord(ev_c[i], stream));
+      cu(cudaStreamWaitEvent(s_out, ev_c[i], 0));
+      for (int n = 0; n < B; ++n) {
+        const size_t off = ((size_t)n * T + t0) * row_qk;
+        cu(cudaMemcpyAsync(static_cast<char*>(out) + off, dout + off, (t1 - t0) * row_qk,
+                           cudaMemcpyDeviceToHost, s_out));
+      }
+    }
+    if (ds1)
+      cu(cudaMemcpyAsync(final_state, ds1, (size_t)B * H * D * D * 4, cudaMemcpyDeviceToHost,
+                         s_out));
+    cu(cudaMemcpyAsync(&hstat, dstat, sizeof(int32_t), cudaMemcpyDeviceToHost, s_out));
+  }
+  // everything queued is waited for, whatever failed
+  for (cudaStream_t sm : {s_in[0], s_in[1], s_out, stream})
+    if (sm || sm == stream) cu(cudaStreamSynchronize(sm));
+  for (int i = 0; i < pieces; ++i) {
+    if (ev_in[0][i]) cudaEventDestroy(ev_in[0][i]);
+    if (ev_in[1][i]) cudaEventDestroy(ev_in[1][i]);
+    if (ev_c[i]) cudaEventDestroy(ev_c[i]);
+  }
+  if (ev0) cudaEventDestroy(ev0);
+  for (cudaStream_t sm : {s_in[0], s_in[1], s_out})
+    if (sm) cudaStreamDestroy(sm);
+  if (st == KDA_OK && hstat != 0) st = (kda_status)hstat;
+  return st;
+}
+}  // namespace
+
+extern "C" {
 
 kda_status kda_chunk_fwd_host(const void* q, const void* k, const void* v, const void* g_logit,
                               const void* beta, const float* init_state, void* out,
@@ -356,8 +477,19 @@ kda_status kda_chunk_fwd_host(const void* q, const void* k, const void* v, const
   float* ds1 = final_state ? (float*)take(s.state) : nullptr;
   int32_t* dcu = packed ? (int32_t*)take(s.cu) : nullptr;
   int32_t* dstat = (int32_t*)take(sizeof(int32_t));
-  const size_t ws_bytes = kda_workspace_bytes(B, T, H, dk, dv, dtype, 0, KDA_ALGO_AUTO, packed);
+  const bool piped = host_pipelined(dtype, dk, dv, packed, T);
+  const size_t ws_bytes =
+      piped ? kda_split_slice_workspace_bytes(B, H, host_piece_chunks(T))
+            : kda_workspace_bytes(B, T, H, dk, dv, dtype, 0, KDA_ALGO_AUTO, packed);
   void* ws = ws_bytes ? take(ws_bytes) : nullptr;
+  if (piped) {
+    kda_status st = host_pipelined_run(q, k, v, g_logit, beta, init_state, out, final_state, B,
+                                       T, H, scale, dq, dk_, dv_, dg, db, ds0, dout, ds1, dstat,
+                                       ws, ws_bytes, stream);
+    if (owned) cudaFreeAsync(base, stream);
+    if (cudaStreamSynchronize(stream) != cudaSuccess && st == KDA_OK) st = KDA_ERR_CUDA;
+    return st;
+  }
   kda_status st = KDA_OK;
   int32_t hstat = 0;
   bool ok = true;

@@ -1014,32 +1014,38 @@ size_t kda_split_min_workspace_bytes(int N, int H) {
 
 namespace {
 
-// The slices run back to back on `stream`; a slice is the intra kernel over
-// its chunks, then the state kernel over the same chunks.  `stages` selects
-// the kernels (bit 0 intra, bit 1 state); `one_slice` refuses a workspace
-// that would need more than one slice.
-kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
-                     cudaStream_t stream, int stages, bool one_slice) {
+// What every slice launch of one call shares: the tensor maps over the
+// inputs, the SM count, and where the records and the carried state live.
+struct SplitPlan {
+  CUtensorMap mq, mk, mg, mv;
+  int sms = 0;
+  int nchunks = 0;
+  size_t carry = 0, per = 0;   // bytes: carried state; records of one chunk column
+  size_t fit = 0;              // chunk columns the workspace holds
+  float* through = nullptr;    // state between slices
+  unsigned char* rec = nullptr;
+};
+
+kda_status plan_split(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
+                      SplitPlan& pl) {
   if (p.cu_seqlens || p.dk != DK || p.dv != DV || p.T < 1) return KDA_ERR_UNSUPPORTED;
   if (p.N > 65535 || p.H > 65535) return KDA_ERR_UNSUPPORTED;
   const int64_t rows = (int64_t)p.N * p.T;
   if (rows >= (int64_t)1 << 31) return KDA_ERR_UNSUPPORTED;
   if (((uintptr_t)workspace & 255) != 0) return KDA_ERR_MISALIGNED;
-  const size_t carry = carry_bytes(p.N, p.H);
-  const size_t per = (size_t)p.N * p.H * REC_BYTES;
-  if (workspace_bytes < carry + per) return KDA_ERR_WORKSPACE;
-  const int nchunks = (int)(((int64_t)p.T + C - 1) / C);
-  const size_t fit = (workspace_bytes - carry) / per;
-  int dev = 0, sms = 0;
+  pl.carry = carry_bytes(p.N, p.H);
+  pl.per = (size_t)p.N * p.H * REC_BYTES;
+  if (workspace_bytes < pl.carry + pl.per) return KDA_ERR_WORKSPACE;
+  pl.nchunks = (int)(((int64_t)p.T + C - 1) / C);
+  pl.fit = (workspace_bytes - pl.carry) / pl.per;
+  int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+      cudaDeviceGetAttribute(&pl.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      pl.sms < 1)
     return KDA_ERR_CUDA;
-  const int slice = fit < (size_t)nchunks ? (int)fit : nchunks;
-  if (one_slice && slice < nchunks) return KDA_ERR_WORKSPACE;
-  CUtensorMap mq, mk, mg, mv;
   // unswizzled tiles: every read of them goes along one row
-  if (!make_map(&mq, p.q, rows, p.H, DK, false) || !make_map(&mk, p.k, rows, p.H, DK, false) ||
-      !make_map(&mg, p.g, rows, p.H, DK, false) || !make_map(&mv, p.v, rows, p.H, DV, false))
+  if (!make_map(&pl.mq, p.q, rows, p.H, DK, false) || !make_map(&pl.mk, p.k, rows, p.H, DK, false) ||
+      !make_map(&pl.mg, p.g, rows, p.H, DK, false) || !make_map(&pl.mv, p.v, rows, p.H, DV, false))
     return KDA_ERR_CUDA;
   static bool attr_set = false;
   if (!attr_set) {
@@ -1052,32 +1058,50 @@ kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_
   }
   // the state crosses slices in final_state when there is one (each CTA
   // reads its part before it writes it), else in the workspace
-  float* ws_carry = static_cast<float*>(workspace);
-  float* through = p.final_state ? p.final_state : ws_carry;
-  unsigned char* rec = static_cast<unsigned char*>(workspace) + carry;
-  for (int c0 = 0; c0 < nchunks; c0 += slice) {
-    const int cnt = nchunks - c0 < slice ? nchunks - c0 : slice;
-    const bool last = c0 + cnt == nchunks;
-    SplitParams sp;
-    sp.p = p;
-    sp.rec = rec;
-    sp.c_begin = c0;
-    sp.c_count = cnt;
-    sp.s_in = c0 == 0 ? p.init_state : through;
-    sp.s_out = last ? p.final_state : through;
-    if (stages & 1) {
-      // persistent: two CTAs per SM walk the slice's (sequence, head, chunk) items
-      const int64_t items = (int64_t)p.N * p.H * cnt;
-      const int grid = items < 2 * (int64_t)sms ? (int)items : 2 * sms;
-      kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(mq, mk, mg, mv, sp);
-      if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-    }
-    if (stages & 2) {
-      kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(sp);
-      if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-    }
+  pl.through = p.final_state ? p.final_state : static_cast<float*>(workspace);
+  pl.rec = static_cast<unsigned char*>(workspace) + pl.carry;
+  return KDA_OK;
+}
+
+// One slice, chunks [c0, c0 + cnt) of every sequence: the intra kernel over
+// it, then the state kernel.  `stages` selects the kernels (bit 0 intra,
+// bit 1 state).
+kda_status launch_slice(const kda::FwdParams& p, const SplitPlan& pl, int c0, int cnt,
+                        cudaStream_t stream, int stages) {
+  SplitParams sp;
+  sp.p = p;
+  sp.rec = pl.rec;
+  sp.c_begin = c0;
+  sp.c_count = cnt;
+  sp.s_in = c0 == 0 ? p.init_state : pl.through;
+  sp.s_out = c0 + cnt == pl.nchunks ? p.final_state : pl.through;
+  if (stages & 1) {
+    // persistent: two CTAs per SM walk the slice's (sequence, head, chunk) items
+    const int64_t items = (int64_t)p.N * p.H * cnt;
+    const int grid = items < 2 * (int64_t)pl.sms ? (int)items : 2 * pl.sms;
+    kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, pl.mv, sp);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+  }
+  if (stages & 2) {
+    kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(sp);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   }
   return KDA_OK;
+}
+
+// The slices run back to back on `stream`; `one_slice` refuses a workspace
+// that would need more than one slice.
+kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream, int stages, bool one_slice) {
+  SplitPlan pl;
+  kda_status st = plan_split(p, workspace, workspace_bytes, pl);
+  if (st != KDA_OK) return st;
+  const int slice = pl.fit < (size_t)pl.nchunks ? (int)pl.fit : pl.nchunks;
+  if (one_slice && slice < pl.nchunks) return KDA_ERR_WORKSPACE;
+  for (int c0 = 0; c0 < pl.nchunks && st == KDA_OK; c0 += slice)
+    st = launch_slice(p, pl, c0, pl.nchunks - c0 < slice ? pl.nchunks - c0 : slice, stream,
+                      stages);
+  return st;
 }
 
 }  // namespace
@@ -1085,6 +1109,25 @@ kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_
 kda_status kda_run_split(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
                          cudaStream_t stream) {
   return run_split(p, workspace, workspace_bytes, stream, 3, false);
+}
+
+// Chunks [c0, c0 + cnt) alone (both kernels); the state enters from
+// init_state (c0 = 0) or from where the previous range left it, and leaves
+// into final_state (last range) or that carry.  The workspace must hold cnt
+// chunk columns of records.
+kda_status kda_run_split_range(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream, int c0, int cnt) {
+  SplitPlan pl;
+  kda_status st = plan_split(p, workspace, workspace_bytes, pl);
+  if (st != KDA_OK) return st;
+  if (c0 < 0 || cnt < 1 || c0 + cnt > pl.nchunks || (size_t)cnt > pl.fit) return KDA_ERR_INVALID_ARG;
+  return launch_slice(p, pl, c0, cnt, stream, 3);
+}
+
+// Device bytes of the two-kernel path for slices of `chunks` chunks.
+size_t kda_split_slice_workspace_bytes(int N, int H, int chunks) {
+  if (N < 1 || H < 1 || chunks < 1) return 0;
+  return carry_bytes(N, H) + (size_t)N * H * REC_BYTES * (size_t)chunks;
 }
 
 extern "C" kda_status kda_split_stage(int stage, const uint16_t* q, const uint16_t* k,

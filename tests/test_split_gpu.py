@@ -180,3 +180,31 @@ def test_full_b2_h32_t32k_split_sampled():
         o_ref, s_ref = oracle.fwd(*args, bt, s0)
         eo, es = rel(o[b, :, h], o_ref[0, :, 0]), rel(s[b, h], s_ref[0, 0])
         assert eo <= 1e-2 and es <= 1e-2, (b, h, eo, es)
+
+
+# ---- the end-to-end entry: pieces copied in, run and copied out in turn ----
+
+@pytest.mark.parametrize("T,s0_std,final", [(1000, 0.02, True), (640, 0.0, True),
+                                            (333, 0.02, False), (65, 0.0, True)])
+def test_host_pipeline_matches_device(T, s0_std, final):
+    """kda_chunk_fwd_host runs the two-kernel path in pieces of whole chunks
+    (inputs of the next piece copied in while the current one runs): the
+    result is bit-identical to the one-call device run."""
+    w = small_workload("hostpipe", B=2, T=T, H=3, dk=128, dv=128, s0_std=s0_std, seed=31)
+    x = make_inputs(w)
+    o_dev, s_dev = run(x, final=final)
+    pin = {k: (v.pin_memory() if torch.is_tensor(v) else v) for k, v in x.items()}
+    out = torch.empty(2, T, 3, 128, dtype=torch.bfloat16).pin_memory()
+    fs = torch.empty(2, 3, 128, 128).pin_memory() if final else None
+    nb = kda.kda_host_staging_bytes(2, T, 3, 128, 128, kda.KDA_BF16,
+                                    int(x["init_state"] is not None), int(final), 0)
+    staging = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    rc = kda.kda_chunk_fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"],
+                                pin["init_state"], out, fs, 2, T, 3, 128, 128, None,
+                                kda.KDA_BF16, 1.0, staging, nb, torch.cuda.current_stream())
+    assert rc == 0, kda.status_string(rc)
+    np.testing.assert_array_equal(out.float().numpy(), o_dev)
+    if final:
+        np.testing.assert_array_equal(fs.numpy(), s_dev)
+    o_ref, s_ref = ref(x)
+    assert rel(out.float().numpy(), o_ref) <= 1e-2
