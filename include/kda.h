@@ -229,7 +229,12 @@ size_t kda_workspace_bytes(int N, int T, int H, int dk, int dv, int dtype, int c
  * pointer here is a host pointer.  dev_buffer: device memory of at least
  * kda_host_staging_bytes() bytes, or NULL (then taken from and returned to
  * the stream-ordered allocator).  The device status is read back and
- * returned as the call's result.
+ * returned as the call's result.  On the two-kernel path (dense bf16,
+ * dk = dv = 128, two or more chunks) the call runs in up to eight pieces of
+ * whole chunks: while piece i runs on `stream`, the inputs of piece i + 1 are
+ * copied in and the output of piece i - 1 copied out on streams of the
+ * call's own, so the copies overlap the kernels; the result is bit-identical
+ * to kda_chunk_fwd_ex on device copies of the same inputs.
  */
 kda_status kda_chunk_fwd_host(const void* q, const void* k, const void* v, const void* g_logit,
                               const void* beta, const float* init_state, void* out,
@@ -238,7 +243,8 @@ kda_status kda_chunk_fwd_host(const void* q, const void* k, const void* v, const
                               void* dev_buffer, size_t dev_buffer_bytes, kda_stream_t stream);
 
 /* Device bytes kda_chunk_fwd_host stages through for these sizes: inputs,
- * outputs, states and the automatic path's workspace. */
+ * outputs, states and the automatic path's workspace (on the two-kernel
+ * path, the chunk records of one piece). */
 size_t kda_host_staging_bytes(int B, int T, int H, int dk, int dv, int dtype, int has_init,
                               int has_final, int packed);
 
