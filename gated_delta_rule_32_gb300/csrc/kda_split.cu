@@ -88,6 +88,7 @@ __device__ __forceinline__ void record_error(const kda::FwdParams& p, int* s_abo
   if (p.dev_status) atomicExch(p.dev_status, (int32_t)st);
 }
 
+
 // ===========================================================================
 // intra kernel
 // ===========================================================================
@@ -104,12 +105,14 @@ constexpr int I_PT = I_BETA + 128;                 // [4 tiles][128] fp32 tile p
 static_assert(I_BETA % 16 == 0, "beta rows are read 8 at a time");
 constexpr int I_BAR = I_PT + 2048;
 constexpr int I_MISC = I_BAR + 64;
-constexpr int I_SMEM = I_MISC + 64;
+constexpr int I_T = I_MISC + 64;                   // T bf16 K-major [r][i] (8192)
+constexpr int I_SMEM = I_T + 8192;
+static_assert(I_T % 16 == 0, "T is an operand and a bulk-copy source");
 // V lands with Q, K, G in the Gram operand buffer, which is free until the
 // first gate pass; the rest overlays what is dead by then
 constexpr int I_V = I_OB;                          // V landing, 2 boxes (until (beta V)^T)
 constexpr int I_AKK = I_OB, I_TF = I_OB + 18432;   // [64][72] fp32 each (after the Grams)
-constexpr int I_T = I_Q, I_Y = I_Q + 8192;         // T bf16 (8192), Y fp32 [32][36]
+constexpr int I_Y = I_Q + 8192;                    // Y fp32 [32][36]
 static_assert(I_V + 16384 <= I_BKG, "V landing");
 static_assert(I_TF + 64 * AKK_LD * 4 <= I_BKG, "solve scratch");
 static_assert(I_Y + 32 * 36 * 4 <= I_K, "block-merge scratch");
@@ -262,6 +265,25 @@ __global__ void __launch_bounds__(kThreads, 2)
     sm100::tc_fence_after();
   };
 
+  // W rows of an item into its record (all warps: lane = key channel, 32
+  // rows each), from tensor memory
+  auto w_out = [&](unsigned char* r) {
+    const int j = tid & 127, rb = (warp >> 2) * 32;
+    float wv[32];
+#pragma unroll
+    for (int c = 0; c < 32; c += 16) {
+      float v[16];
+      sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_W + rb + c), v);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) wv[c + e] = v[e];
+    }
+    sm100::tmem_wait_ld();
+#pragma unroll
+    for (int rg = 0; rg < 4; ++rg)
+      st8_bf16(r + REC_WQ + mn_off(rb + 8 * rg, j, 2048), wv + 8 * rg);
+  };
+  unsigned char* w_rec = nullptr;  // item whose W product is in flight
+
   for (int li = 0; cur.w < n_items; ++li) {
     const int L = cur.L;
     unsigned char* rec = sp.rec + cur.w * (int64_t)REC_BYTES;
@@ -307,12 +329,21 @@ __global__ void __launch_bounds__(kThreads, 2)
       s_pt[a * 128 + 64 + jl] = p1;
     }
     sm100::fence_async_smem();
-    __syncthreads();
-    if (*s_abort) break;
+    if (sync_aborted(s_abort)) break;
     // the decay logits live on in registers only: the next item's G tiles
     if (has_next) {
       if (tid == 32) load_g(nxt);
       g_issued = li + 2;
+    }
+    // the previous item's W product, then its rows into that record; its T
+    // copy has left shared memory before this item's solve rewrites it
+    // (a thread that saw the wait fail skips the rows; the loop leaves at
+    // the next check that follows a barrier)
+    if (w_rec) {
+      wait_mma();
+      if (!*s_abort) w_out(w_rec);
+      w_rec = nullptr;
+      if (tid == 32) sm100::bulk_wait_read();
     }
     // (beta V)^T, K-major [value channel jv][row r], into the record; V is
     // read before the gate passes overwrite it
@@ -489,9 +520,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     SPLIT_MARK(4, mk);
     gate_pass(al1, 1);
     sm100::fence_async_smem();
-    sync_all();
+    if (sync_aborted(s_abort)) break;
     SPLIT_MARK(5, mk);
-    if (*s_abort) break;
     // K has been read for the last time: the next item's K tiles
     if (has_next) {
       if (tid == 32) load_k(nxt);
@@ -581,9 +611,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     sm100::fence_async_smem();
-    sync_all();
+    if (sync_aborted(s_abort)) break;
     SPLIT_MARK(7, mk);
-    if (*s_abort) break;
 
     // ---- T = (I + beta A_kk)^{-1} -------------------------------------------
     unit_lower_inverse<AKK_LD>(s_akk, reinterpret_cast<float*>(smem + I_TF),
@@ -591,16 +620,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     sm100::fence_async_smem();
     sync_all();
     SPLIT_MARK(8, mk);
-    // T into the record by one bulk copy (read out of shared memory before
-    // the next item's Q lands there); the solve scratch (over V's landing
-    // zone) is dead: the next item's V tiles
+    // T into the record by one bulk copy; the solve scratch (over V's and
+    // Q's landing zones) is dead: the next item's V and Q tiles
     if (tid == 32) {
       sm100::bulk_store(rec + REC_T, smem + I_T, 8192);
       sm100::bulk_commit();
     }
     if (has_next) {
-      if (tid == 32) load_v(nxt);
+      if (tid == 32) {
+        load_v(nxt);
+        load_q(nxt);
+      }
       v_issued = li + 2;
+      q_issued = li + 2;
     }
 
     // ---- W^T = (beta K gamma)^T T^T (U = T (beta V) is formed by the state
@@ -615,36 +647,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                       sm100::smem_desc(s_t + 256 * s, 128, 1024), idw, s > 0);
       sm100::mma_commit(bar_mma);
     }
+    // the product is waited for (and W read out) after the next item's
+    // decay map, which it overlaps
     mma_pending = true;
-    wait_mma();
+    w_rec = rec;
     SPLIT_MARK(9, mk);
-    if (*s_abort) break;
-    // T (over Q) is dead once its copy to the record has read it: the next
-    // item's Q tiles
-    if (has_next) {
-      if (tid == 32) {
-        sm100::bulk_wait_read();
-        load_q(nxt);
-      }
-      q_issued = li + 2;
-    }
-
-    // ---- record: W rows (all warps: lane = key channel, 32 rows each) -----
-    {
-      const int j = tid & 127, rb = (warp >> 2) * 32;
-      float wv[32];
-#pragma unroll
-      for (int c = 0; c < 32; c += 16) {
-        float v[16];
-        sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_W + rb + c), v);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) wv[c + e] = v[e];
-      }
-      sm100::tmem_wait_ld();
-#pragma unroll
-      for (int rg = 0; rg < 4; ++rg)
-        st8_bf16(rec + REC_WQ + mn_off(rb + 8 * rg, j, 2048), wv + 8 * rg);
-    }
     SPLIT_MARK(10, mk);
 #ifdef KDA_PHASE_TIMING
     if (mk) atomicAdd(&kda_split_cycles[12], 1ull);  // items measured
@@ -652,6 +659,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     cur = nxt;
   }
 
+  // the last item's W product
+  if (!*s_abort && w_rec) {
+    wait_mma();
+    if (!*s_abort) w_out(w_rec);
+  }
   // after an abort: bounded waits for copies and products still in flight
   // before the shared and tensor memory are released (at most one copy per
   // barrier is outstanding)
@@ -848,6 +860,8 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
     sm100::fence_async_smem();
     sync_all();
     SPLIT_MARK(18, mk);
+    // (checks right after a barrier: a flag raised after it needs a wait that
+    // timed out, seconds after every thread has read it here)
     if (*s_abort) break;
 
     // (2) P = [W; Q gamma] S

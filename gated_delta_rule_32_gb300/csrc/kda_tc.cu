@@ -323,9 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       gate_alpha(0);  // later chunks: computed while the previous chunk's P runs
     }
     KDA_PHASE(11);
-    __syncthreads();
+    const bool aborted = sync_aborted(s_abort);
     KDA_PHASE(0);
-    if (*s_abort) break;
+    if (aborted) break;
 
     // ---- (B) gate: one key channel j, one half (two tiles) per thread -------
     {
@@ -798,9 +798,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    sync_all();
+    const bool aborted_end = sync_aborted(s_abort);
     KDA_PHASE(10);
-    if (*s_abort) break;
+    if (aborted_end) break;
   }
 
   // ---- drain anything still in flight after an abort, write the state ----

@@ -249,6 +249,17 @@ __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, fl
   }
 }
 
+// A CTA barrier (with the tensor-core ordering fences) that also makes every
+// thread agree on whether any thread has recorded an error: a thread that
+// runs ahead and fails a later wait cannot make the others leave the loop
+// at different points.
+__device__ __forceinline__ bool sync_aborted(const int* s_abort) {
+  sm100::tc_fence_before();
+  const int any = __syncthreads_or(*reinterpret_cast<const volatile int*>(s_abort));
+  sm100::tc_fence_after();
+  return any != 0;
+}
+
 // ---------------------------------------------------------------------------
 // host: TMA tensor maps
 inline PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
