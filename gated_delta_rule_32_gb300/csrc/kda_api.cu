@@ -6,6 +6,8 @@
 
 #include "kda_common.cuh"
 
+size_t kda_split_packed_workspace_bytes(int N, int T, int H);
+
 namespace {
 
 bool dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
@@ -91,13 +93,22 @@ bool use_tc(int dtype, int dk, int dv, int chunk_size, int algo) {
   return kda_tc_supported(dk, dv);
 }
 
-// The two-kernel form of the tensor-core path: dense batches, when asked for
-// or by default (it runs every chunk's state-independent work at once; the
-// fused kernel, which repeats it per value half and runs it serially per
-// chain, stays the path of packed batches and of KDA_ALGO_TC).
-bool use_split(int dtype, int dk, int dv, int chunk_size, int algo, int packed, int T) {
-  if (packed || T < 1 || !use_tc(dtype, dk, dv, chunk_size, algo)) return false;
-  return algo == KDA_ALGO_SPLIT || algo == KDA_ALGO_AUTO;
+// The two-kernel form of the tensor-core path, when asked for or by default
+// (it runs every chunk's state-independent work at once; the fused kernel
+// repeats it per value half and runs it serially per chain).  A packed batch
+// keeps all its chunk records at once, so by default it takes this form only
+// while they fit in 4 GiB, else the fused kernel; KDA_ALGO_TC always takes
+// the fused kernel.
+bool use_split(int dtype, int dk, int dv, int chunk_size, int algo, int packed, int N, int T,
+               int H) {
+  if (T < 1 || !use_tc(dtype, dk, dv, chunk_size, algo)) return false;
+  if (algo != KDA_ALGO_SPLIT && algo != KDA_ALGO_AUTO) return false;
+  if (packed) {
+    if (N < 1 || N >= (1 << 24)) return false;
+    if (algo == KDA_ALGO_AUTO && kda_split_packed_workspace_bytes(N, T, H) > ((size_t)4 << 30))
+      return false;
+  }
+  return true;
 }
 
 }  // namespace
@@ -127,18 +138,22 @@ int host_piece_chunks(int T) {
   return (nchunks + pieces - 1) / pieces;
 }
 bool host_pipelined(int dtype, int dk, int dv, int packed, int T) {
-  return use_split(dtype, dk, dv, 0, KDA_ALGO_AUTO, packed, T) && (T + 63) / 64 >= 2;
+  return !packed && use_split(dtype, dk, dv, 0, KDA_ALGO_AUTO, 0, 1, T, 1) && (T + 63) / 64 >= 2;
 }
 }  // namespace
 // A workspace smaller than the default (but at least the minimum) runs the
 // sequence in more, shorter slices.
 static kda_status run_split_ws(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream) {
+  const bool packed = p.cu_seqlens != nullptr;  // (all records at once: no slices)
   if (workspace) {
-    if (workspace_bytes < kda_split_min_workspace_bytes(p.N, p.H)) return KDA_ERR_WORKSPACE;
+    const size_t min_bytes = packed ? kda_split_packed_workspace_bytes(p.N, p.T, p.H)
+                                    : kda_split_min_workspace_bytes(p.N, p.H);
+    if (workspace_bytes < min_bytes) return KDA_ERR_WORKSPACE;
     return kda_run_split(p, workspace, workspace_bytes, stream);
   }
-  const size_t need = kda_split_workspace_bytes(p.N, p.T, p.H);
+  const size_t need = packed ? kda_split_packed_workspace_bytes(p.N, p.T, p.H)
+                             : kda_split_workspace_bytes(p.N, p.T, p.H);
   void* ws = nullptr;
   if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return KDA_ERR_CUDA;
   kda_status st = kda_run_split(p, ws, need, stream);
@@ -198,16 +213,17 @@ int kda_resolve_path(int N, int T, int H, int dk, int dv, int dtype, int chunk_s
   if (fam < 0 || N < 1 || H < 1 || T < 0) return -1;
   if (fam == KDA_ALGO_SIMT) return KDA_ALGO_SIMT;
   if (algo == KDA_ALGO_TC) return KDA_ALGO_TC;
-  if (!use_split(dtype, dk, dv, chunk_size, algo, packed, T)) return KDA_ALGO_TC;
+  if (!use_split(dtype, dk, dv, chunk_size, algo, packed, N, T, H)) return KDA_ALGO_TC;
   return KDA_ALGO_SPLIT;
 }
 
 size_t kda_workspace_bytes(int N, int T, int H, int dk, int dv, int dtype, int chunk_size,
                            int algo, int packed) {
-  if (packed || N < 1 || H < 1 || T < 1) return 0;
+  if (N < 1 || H < 1 || T < 1) return 0;
   if (!use_tc(dtype, dk, dv, chunk_size, algo)) return 0;
-  if (use_split(dtype, dk, dv, chunk_size, algo, packed, T))
-    return kda_split_workspace_bytes(N, T, H);
+  if (use_split(dtype, dk, dv, chunk_size, algo, packed, N, T, H))
+    return packed ? kda_split_packed_workspace_bytes(N, T, H) : kda_split_workspace_bytes(N, T, H);
+  if (packed) return 0;
   const int nseg = auto_segments(N, T, H, sm_count());
   return nseg > 1 ? kda_seg_scratch_bytes(N, H, nseg, dk, dv) : 0;
 }
@@ -267,10 +283,10 @@ static kda_status fwd_impl(const void* q, const void* k, const void* v, const vo
   p.ckpt = ckpt; p.ckpt_every = ckpt_every; p.ckpt_max = ckpt_max;
   if ((algo == KDA_ALGO_TC || algo == KDA_ALGO_SPLIT) && !use_tc(dtype, dk, dv, chunk_size, algo))
     return KDA_ERR_UNSUPPORTED;
-  if (algo == KDA_ALGO_SPLIT && cu_seqlens) return KDA_ERR_UNSUPPORTED;
   if (!use_tc(dtype, dk, dv, chunk_size, algo)) return kda_launch_simt(p, dtype, stream);
-  if (use_split(dtype, dk, dv, chunk_size, algo, cu_seqlens != nullptr, T))
+  if (use_split(dtype, dk, dv, chunk_size, algo, cu_seqlens != nullptr, B, T, H))
     return run_split_ws(p, workspace, workspace_bytes, stream);
+  if (algo == KDA_ALGO_SPLIT) return KDA_ERR_UNSUPPORTED;
   const int nseg = (cu_seqlens || ckpt) ? 1 : auto_segments(B, T, H, sm_count());
   if (nseg <= 1) return kda_launch_tc(p, stream);
   return run_segmented_ws(p, nseg, workspace, workspace_bytes, stream);

@@ -58,11 +58,17 @@ static_assert(ST_BV == ST_T + 8192 && REC_BV == REC_T + 8192, "U operand rows");
 
 struct SplitParams {
   kda::FwdParams p;
-  unsigned char* rec;  // records [N][H][c_count]
-  int c_begin;         // first chunk of the slice
-  int c_count;         // chunks in the slice
+  unsigned char* rec;  // records: dense [N][H][c_count], packed [H][g_max]
+  int c_begin;         // first chunk of the slice (dense)
+  int c_count;         // chunks in the slice (dense)
   const float* s_in;   // state entering the slice [N][H][DK][DV] (null: zero)
   float* s_out;        // state leaving the slice (null: not kept)
+  // packed batches (cu_seqlens; one slice): sequence n owns the chunk
+  // columns [chunk_off[n], chunk_off[n + 1]); column g starts at token row
+  // chunk_tab[g].x and holds chunk_tab[g].y >> 24 rows (0: no chunk)
+  const int2* chunk_tab;  // [g_max], null for dense batches
+  const int* chunk_off;   // [N + 1]
+  int g_max;              // chunk columns: ceil(T / 64) + N bounds the true count
 };
 
 #ifdef KDA_PHASE_TIMING
@@ -130,46 +136,72 @@ __global__ void __launch_bounds__(kThreads, 2)
   const kda::FwdParams& p = sp.p;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int H = p.H;
-  // work items: w = (n * H + h) * c_count + chunk of the slice; this CTA
-  // takes blockIdx.x, blockIdx.x + gridDim.x, ...
-  const int64_t n_items = (int64_t)p.N * H * sp.c_count;
+  // work items: dense w = (n * H + h) * c_count + chunk of the slice,
+  // packed w = chunk column * H + h; this CTA takes blockIdx.x,
+  // blockIdx.x + gridDim.x, ...
+  const bool packed = sp.chunk_tab != nullptr;
+  const int64_t n_items = packed ? (int64_t)sp.g_max * H : (int64_t)p.N * H * sp.c_count;
   struct Item {
-    int n, h, cl;    // sequence, head, chunk of the slice
+    int n, h, cl;    // sequence, head, chunk of the slice (packed: chunk column)
     int L;           // valid rows of the chunk
     int64_t row0;    // global row of its first token
     int64_t w;
+    int64_t ri;      // its record
   };
   auto finish = [&](Item& it) {
-    const int64_t cs = ((int64_t)sp.c_begin + it.cl) * C;
-    it.L = (p.T - cs) < C ? (int)(p.T - cs) : C;
-    it.row0 = (int64_t)it.n * p.T + cs;
+    if (packed) {  // (read well before its first use, the next item's tiles)
+      const int2 e = it.w < n_items ? sp.chunk_tab[it.cl] : make_int2(0, 0);
+      it.row0 = e.x;
+      it.n = e.y & 0xFFFFFF;
+      it.L = (e.y >> 24) & 0x7F;
+      it.ri = (int64_t)it.h * sp.g_max + it.cl;
+    } else {
+      const int64_t cs = ((int64_t)sp.c_begin + it.cl) * C;
+      it.L = (p.T - cs) < C ? (int)(p.T - cs) : C;
+      it.row0 = (int64_t)it.n * p.T + cs;
+      it.ri = it.w;
+    }
   };
   // the coordinates of item w (divisions: once per CTA), and those of the
   // item gridDim.x further on, by carries (32-bit adds only)
   auto item_of = [&](int64_t w) {
     Item it;
-    const int nh = (int)(w / sp.c_count);
-    it.cl = (int)(w % sp.c_count);
-    it.h = nh % H;
-    it.n = nh / H;
+    if (packed) {
+      it.h = (int)(w % H);
+      it.cl = (int)(w / H);
+      it.n = 0;
+    } else {
+      const int nh = (int)(w / sp.c_count);
+      it.cl = (int)(w % sp.c_count);
+      it.h = nh % H;
+      it.n = nh / H;
+    }
     it.w = w;
     finish(it);
     return it;
   };
-  const int step_cl = (int)(gridDim.x % sp.c_count);
-  const int step_nh = (int)(gridDim.x / sp.c_count);
-  const int step_h = step_nh % H, step_n = step_nh / H;
+  const int step_cl = packed ? (int)(gridDim.x / H) : (int)(gridDim.x % sp.c_count);
+  const int step_nh = packed ? 0 : (int)(gridDim.x / sp.c_count);
+  const int step_h = packed ? (int)(gridDim.x % H) : step_nh % H, step_n = step_nh / H;
   auto next_of = [&](const Item& a) {
     Item it;
     it.w = a.w + gridDim.x;
-    it.cl = a.cl + step_cl;
-    const int carry = it.cl >= sp.c_count;
-    if (carry) it.cl -= sp.c_count;
-    it.h = a.h + step_h + carry;
-    it.n = a.n + step_n;
-    if (it.h >= H) {
-      it.h -= H;
-      it.n += 1;
+    if (packed) {
+      it.h = a.h + step_h;
+      const int carry = it.h >= H;
+      if (carry) it.h -= H;
+      it.cl = a.cl + step_cl + carry;
+      it.n = 0;
+    } else {
+      it.cl = a.cl + step_cl;
+      const int carry = it.cl >= sp.c_count;
+      if (carry) it.cl -= sp.c_count;
+      it.h = a.h + step_h + carry;
+      it.n = a.n + step_n;
+      if (it.h >= H) {
+        it.h -= H;
+        it.n += 1;
+      }
     }
     finish(it);
     return it;
@@ -286,15 +318,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   for (int li = 0; cur.w < n_items; ++li) {
     const int L = cur.L;
-    unsigned char* rec = sp.rec + cur.w * (int64_t)REC_BYTES;
+    unsigned char* rec = sp.rec + cur.ri * (int64_t)REC_BYTES;
     const Item nxt = next_of(cur);
     const bool has_next = nxt.w < n_items;
     const uint32_t par = (uint32_t)(li & 1);
     if (!sm100::mbar_wait(bar_g, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
     else g_done = li + 1;
     if (tid < C) s_beta_raw[tid] = beta_raw;  // bf16 bits; readers widen them
-    // the next item's beta, a whole item ahead of its use
-    if (has_next) beta_raw = load_beta(nxt);
     // rows past the end of the sequence (its last chunk only): a decay logit
     // far below zero (alpha = 1), so that no later step masks
     if (L < C) {
@@ -330,10 +360,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     sm100::fence_async_smem();
     if (sync_aborted(s_abort)) break;
-    // the decay logits live on in registers only: the next item's G tiles
+    // the decay logits live on in registers only: the next item's G tiles,
+    // and its beta (an item ahead of its use)
     if (has_next) {
       if (tid == 32) load_g(nxt);
       g_issued = li + 2;
+      beta_raw = load_beta(nxt);
     }
     // the previous item's W product, then its rows into that record; its T
     // copy has left shared memory before this item's solve rewrites it
@@ -700,13 +732,27 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
   const kda::FwdParams& p = sp.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int half = blockIdx.x, h = blockIdx.y, n = blockIdx.z, H = p.H;
-  const int nc = sp.c_count;
 #ifdef KDA_PHASE_TIMING
   long long t_mark = clock64();
   const bool mk = tid == 0 && half == 0 && h == 0 && n == 0;
 #endif
-  const unsigned char* rec0 =
-      sp.rec + ((int64_t)n * H + h) * (int64_t)sp.c_count * REC_BYTES;
+  // this sequence: its chunks (of the slice), records, first token row and
+  // length
+  int nc;
+  int64_t row_base, seq_len;
+  const unsigned char* rec0;
+  if (sp.chunk_tab) {
+    const int c_lo = sp.chunk_off[n];
+    nc = sp.chunk_off[n + 1] - c_lo;
+    row_base = p.cu_seqlens[n];
+    seq_len = p.cu_seqlens[n + 1] - row_base;
+    rec0 = sp.rec + ((int64_t)h * sp.g_max + c_lo) * REC_BYTES;
+  } else {
+    nc = sp.c_count;
+    row_base = (int64_t)n * p.T;
+    seq_len = p.T;
+    rec0 = sp.rec + ((int64_t)n * H + h) * (int64_t)sp.c_count * REC_BYTES;
+  }
   const int64_t sbase = ((int64_t)n * H + h) * (int64_t)DK * DV + half * 64;
 
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem + S_BAR);  // [2]
@@ -782,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
   auto write_out = [&](int c) {
     const int r = tid - 192;
     const int64_t cs = ((int64_t)sp.c_begin + c) * C;
-    const int L = (p.T - cs) < C ? (int)(p.T - cs) : C;
+    const int L = (seq_len - cs) < C ? (int)(seq_len - cs) : C;
     float o[64];
 #pragma unroll
     for (int c16 = 0; c16 < 64; c16 += 16) {
@@ -794,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
     sm100::tmem_wait_ld();
     if (r < L) {
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) +
-                           (((int64_t)n * p.T + cs + r) * H + h) * DV + half * 64;
+                           ((row_base + cs + r) * H + h) * DV + half * 64;
 #pragma unroll
       for (int g = 0; g < 8; ++g) {
         const uint4 w = make_uint4(sm100::pack_bf16x2(o[8 * g], o[8 * g + 1]),
@@ -937,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
     //     ahead of the next chunk's rescaling)
     if (p.ckpt) {
       const int64_t cs = ((int64_t)sp.c_begin + c) * C;
-      const int L = (p.T - cs) < C ? (int)(p.T - cs) : C;
+      const int L = (seq_len - cs) < C ? (int)(seq_len - cs) : C;
       const int64_t done = cs + L;
       if (L == C && done % p.ckpt_every == 0 && done / p.ckpt_every <= p.ckpt_max) {
         const int i = tid & 127, cb = (warp >> 2) * 32;
@@ -988,13 +1034,114 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
   if (warp == 0) sm100::tmem_dealloc(tmem, S_TM_COLS);
 }
 
+// ===========================================================================
+// packed batches: the chunk columns of the sequences
+// ===========================================================================
+// One CTA: off[n] = chunks of the sequences before n (an exclusive scan of
+// ceil(len / 64)), off[N] = their total.  Malformed offsets (cu[0] != 0,
+// cu[N] != T, a decreasing pair) are reported through the status word and
+// leave every sequence without chunks.
+__global__ void __launch_bounds__(1024)
+    kda_split_offsets_kernel(const int32_t* cu, int N, int T, int* off, int32_t* dev_status) {
+  __shared__ int s_bad, s_carry, s_warp[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_bad = (cu[0] != 0 || cu[N] != T) ? 1 : 0;
+    s_carry = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < N; base += 1024) {
+    const int n = base + tid;
+    int cnt = 0;
+    if (n < N) {
+      const int len = cu[n + 1] - cu[n];
+      if (len < 0) s_bad = 1;  // (every writer stores the same value)
+      else cnt = (len + C - 1) / C;
+    }
+    int x = cnt;  // inclusive scan: within the warp, then over the warps
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, d);
+      if (lane >= d) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int wv = s_warp[lane];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wv, d);
+        if (lane >= d) wv += y;
+      }
+      s_warp[lane] = wv;
+    }
+    __syncthreads();
+    if (n < N) off[n] = s_carry + (warp ? s_warp[warp - 1] : 0) + x - cnt;
+    __syncthreads();
+    if (tid == 0) s_carry += s_warp[31];
+    __syncthreads();
+  }
+  if (s_bad) {
+    for (int n = tid; n <= N; n += 1024) off[n] = 0;
+    if (tid == 0 && dev_status) atomicExch(dev_status, (int32_t)KDA_ERR_BAD_SEQLENS);
+  } else if (tid == 0) {
+    off[N] = s_carry;
+  }
+}
+
+// tab[g] for every chunk column g < g_max: {first token row, n | rows << 24}
+// of the chunk there ({0, 0} past the last one); n by bisection over off
+__global__ void kda_split_table_kernel(const int32_t* cu, const int* off, int N, int g_max,
+                                       int2* tab) {
+  const int total = off[N];
+  for (int g = blockIdx.x * blockDim.x + threadIdx.x; g < g_max; g += gridDim.x * blockDim.x) {
+    int2 e = make_int2(0, 0);
+    if (g < total) {
+      int lo = 0, hi = N - 1;  // the last n with off[n] <= g
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= g) lo = mid;
+        else hi = mid - 1;
+      }
+      const int cl = g - off[lo];
+      const int len = cu[lo + 1] - cu[lo];
+      const int L = len - cl * C < C ? len - cl * C : C;
+      e = make_int2(cu[lo] + cl * C, lo | (L << 24));
+    }
+    tab[g] = e;
+  }
+}
+
 // default bytes of records held at once (the slice length follows from it)
 constexpr size_t kRecordBudget = (size_t)4 << 30;
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t carry_bytes(int N, int H) { return align256((size_t)N * H * DK * DV * sizeof(float)); }
 
+// packed batches, one slice: [carry][chunk_off: N + 1 ints][chunk_tab:
+// g_max entries][records: H x g_max]
+int packed_g_max(int N, int T) { return (int)(((int64_t)T + C - 1) / C + N); }
+struct PackedLayout {
+  size_t off_at, tab_at, rec_at, total;
+};
+PackedLayout packed_layout(int N, int T, int H) {
+  PackedLayout L;
+  const size_t g = (size_t)packed_g_max(N, T);
+  L.off_at = carry_bytes(N, H);
+  L.tab_at = L.off_at + align256((size_t)(N + 1) * sizeof(int));
+  L.rec_at = L.tab_at + align256(g * sizeof(int2));
+  L.total = L.rec_at + g * (size_t)H * REC_BYTES;
+  return L;
+}
+
 }  // namespace
+
+// Device bytes of the two-kernel path for a packed batch of T tokens in N
+// sequences (all chunk records at once).
+size_t kda_split_packed_workspace_bytes(int N, int T, int H) {
+  if (N < 1 || H < 1 || T < 1) return 0;
+  return packed_layout(N, T, H).total;
+}
 
 #ifdef KDA_PHASE_TIMING
 extern "C" int kda_split_timing_read(unsigned long long* out32, int reset) {
@@ -1038,20 +1185,35 @@ struct SplitPlan {
   size_t fit = 0;              // chunk columns the workspace holds
   float* through = nullptr;    // state between slices
   unsigned char* rec = nullptr;
+  // packed batches
+  bool packed = false;
+  int g_max = 0;
+  int* chunk_off = nullptr;
+  int2* chunk_tab = nullptr;
 };
 
 kda_status plan_split(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
                       SplitPlan& pl) {
-  if (p.cu_seqlens || p.dk != DK || p.dv != DV || p.T < 1) return KDA_ERR_UNSUPPORTED;
+  pl.packed = p.cu_seqlens != nullptr;
+  if (p.dk != DK || p.dv != DV || p.T < 1) return KDA_ERR_UNSUPPORTED;
   if (p.N > 65535 || p.H > 65535) return KDA_ERR_UNSUPPORTED;
-  const int64_t rows = (int64_t)p.N * p.T;
+  const int64_t rows = pl.packed ? (int64_t)p.T : (int64_t)p.N * p.T;
   if (rows >= (int64_t)1 << 31) return KDA_ERR_UNSUPPORTED;
   if (((uintptr_t)workspace & 255) != 0) return KDA_ERR_MISALIGNED;
   pl.carry = carry_bytes(p.N, p.H);
-  pl.per = (size_t)p.N * p.H * REC_BYTES;
-  if (workspace_bytes < pl.carry + pl.per) return KDA_ERR_WORKSPACE;
-  pl.nchunks = (int)(((int64_t)p.T + C - 1) / C);
-  pl.fit = (workspace_bytes - pl.carry) / pl.per;
+  if (pl.packed) {
+    const PackedLayout L = packed_layout(p.N, p.T, p.H);
+    if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    pl.g_max = packed_g_max(p.N, p.T);
+    pl.chunk_off = reinterpret_cast<int*>(ws + L.off_at);
+    pl.chunk_tab = reinterpret_cast<int2*>(ws + L.tab_at);
+  } else {
+    pl.per = (size_t)p.N * p.H * REC_BYTES;
+    if (workspace_bytes < pl.carry + pl.per) return KDA_ERR_WORKSPACE;
+    pl.nchunks = (int)(((int64_t)p.T + C - 1) / C);
+    pl.fit = (workspace_bytes - pl.carry) / pl.per;
+  }
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&pl.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -1070,6 +1232,11 @@ kda_status plan_split(const kda::FwdParams& p, void* workspace, size_t workspace
       return KDA_ERR_CUDA;
     attr_set = true;
   }
+  if (pl.packed) {
+    pl.rec = static_cast<unsigned char*>(workspace) + packed_layout(p.N, p.T, p.H).rec_at;
+    pl.through = nullptr;
+    return KDA_OK;
+  }
   // the state crosses slices in final_state when there is one (each CTA
   // reads its part before it writes it), else in the workspace
   pl.through = p.final_state ? p.final_state : static_cast<float*>(workspace);
@@ -1087,6 +1254,9 @@ kda_status launch_slice(const kda::FwdParams& p, const SplitPlan& pl, int c0, in
   sp.rec = pl.rec;
   sp.c_begin = c0;
   sp.c_count = cnt;
+  sp.chunk_tab = nullptr;
+  sp.chunk_off = nullptr;
+  sp.g_max = 0;
   sp.s_in = c0 == 0 ? p.init_state : pl.through;
   sp.s_out = c0 + cnt == pl.nchunks ? p.final_state : pl.through;
   if (stages & 1) {
@@ -1105,11 +1275,41 @@ kda_status launch_slice(const kda::FwdParams& p, const SplitPlan& pl, int c0, in
 
 // The slices run back to back on `stream`; `one_slice` refuses a workspace
 // that would need more than one slice.
+// A packed batch in one slice: its chunk table, then both kernels over every
+// chunk column.
+kda_status launch_packed(const kda::FwdParams& p, const SplitPlan& pl, cudaStream_t stream) {
+  kda_split_offsets_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.N, p.T, pl.chunk_off,
+                                                   p.dev_status);
+  const int tb_need = (pl.g_max + 255) / 256;
+  const int tb = tb_need < 8 * pl.sms ? tb_need : 8 * pl.sms;
+  kda_split_table_kernel<<<tb, 256, 0, stream>>>(p.cu_seqlens, pl.chunk_off, p.N, pl.g_max,
+                                                 pl.chunk_tab);
+  if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+  SplitParams sp;
+  sp.p = p;
+  sp.rec = pl.rec;
+  sp.c_begin = 0;
+  sp.c_count = 0;
+  sp.s_in = p.init_state;
+  sp.s_out = p.final_state;
+  sp.chunk_tab = pl.chunk_tab;
+  sp.chunk_off = pl.chunk_off;
+  sp.g_max = pl.g_max;
+  const int64_t items = (int64_t)pl.g_max * p.H;
+  const int grid = items < 2 * (int64_t)pl.sms ? (int)items : 2 * pl.sms;
+  kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, pl.mv, sp);
+  if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+  kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(sp);
+  if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+  return KDA_OK;
+}
+
 kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
                      cudaStream_t stream, int stages, bool one_slice) {
   SplitPlan pl;
   kda_status st = plan_split(p, workspace, workspace_bytes, pl);
   if (st != KDA_OK) return st;
+  if (pl.packed) return stages == 3 ? launch_packed(p, pl, stream) : KDA_ERR_UNSUPPORTED;
   const int slice = pl.fit < (size_t)pl.nchunks ? (int)pl.fit : pl.nchunks;
   if (one_slice && slice < pl.nchunks) return KDA_ERR_WORKSPACE;
   for (int c0 = 0; c0 < pl.nchunks && st == KDA_OK; c0 += slice)
@@ -1131,6 +1331,7 @@ kda_status kda_run_split(const kda::FwdParams& p, void* workspace, size_t worksp
 // chunk columns of records.
 kda_status kda_run_split_range(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream, int c0, int cnt) {
+  if (p.cu_seqlens) return KDA_ERR_UNSUPPORTED;
   SplitPlan pl;
   kda_status st = plan_split(p, workspace, workspace_bytes, pl);
   if (st != KDA_OK) return st;

@@ -100,14 +100,18 @@ def test_package_fails_loudly_without_library(tmp_path):
 
 def test_split_path_host_checks(lib):
     # workspace sizing of the two-kernel path: carried state + one slice of
-    # 82432-byte chunk records per (sequence, head); packed batches need none
+    # 82432-byte chunk records per (sequence, head); a packed batch keeps
+    # every chunk column (ceil(T / 64) + N of them at most) at once, after
+    # its chunk offsets and chunk table
     carry = 2 * 32 * 128 * 128 * 4
     nb = kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=kda.KDA_ALGO_SPLIT)
     assert nb == carry + 2 * 32 * 512 * 82432
     assert kda.kda_workspace_bytes(2, 100, 1, 128, 128, algo=kda.KDA_ALGO_SPLIT) == \
         2 * 128 * 128 * 4 + 2 * 2 * 82432
+    g_max = 32768 // 64 + 2
     assert kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=kda.KDA_ALGO_SPLIT,
-                                   packed=1) == 0
+                                   packed=1) == carry + 256 + 4352 + 32 * g_max * 82432
+    assert g_max * 8 <= 4352
     assert kda.kda_resolve_algo(kda.KDA_BF16, 128, 128, 0, kda.KDA_ALGO_SPLIT) == \
         kda.KDA_ALGO_SPLIT
     assert kda.kda_resolve_algo(kda.KDA_BF16, 64, 128, 0, kda.KDA_ALGO_SPLIT) == -1
@@ -121,11 +125,13 @@ def test_split_path_host_checks(lib):
 
 
 def test_resolve_path(lib):
-    # the automatic path of a dense bf16 batch is the two-kernel form, packed
-    # batches take the fused kernel, fp32 inputs the CUDA-core path
+    # the automatic path of a bf16 batch is the two-kernel form (a packed one
+    # while all its chunk records fit in 4 GiB, else the fused kernel), fp32
+    # inputs take the CUDA-core path
     rp = kda.kda_resolve_path
     assert rp(2, 32768, 32) == kda.KDA_ALGO_SPLIT
-    assert rp(2, 32768, 32, packed=True) == kda.KDA_ALGO_TC
+    assert rp(2, 32768, 32, packed=True) == kda.KDA_ALGO_SPLIT
+    assert rp(1, 1 << 20, 16, packed=True) == kda.KDA_ALGO_TC
     assert rp(2, 32768, 32, algo=kda.KDA_ALGO_TC) == kda.KDA_ALGO_TC
     assert rp(2, 100, 4, dtype=kda.KDA_F32) == kda.KDA_ALGO_SIMT
     assert rp(2, 100, 4, dk=64) == kda.KDA_ALGO_SIMT

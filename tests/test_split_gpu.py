@@ -137,12 +137,14 @@ def test_workspace_too_small_is_refused():
                               2, 128, 128, None, kda.KDA_BF16, 0, 1.0, SPLIT, ws, nb, None,
                               torch.cuda.current_stream())
     assert rc == kda.KDA_ERR_WORKSPACE
-    # packed batches are not taken by the two-kernel path
+    # a packed batch needs all its chunk records at once
     cu = torch.tensor([0, 100, 128], dtype=torch.int32, device="cuda")
+    need = kda.kda_workspace_bytes(2, 128, 2, 128, 128, algo=SPLIT, packed=1)
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
     rc = kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], None, out, None, 2, 128,
-                              2, 128, 128, cu, kda.KDA_BF16, 0, 1.0, SPLIT, None, 0, None,
+                              2, 128, 128, cu, kda.KDA_BF16, 0, 1.0, SPLIT, ws, need - 256, None,
                               torch.cuda.current_stream())
-    assert rc == kda.KDA_ERR_UNSUPPORTED
+    assert rc == kda.KDA_ERR_WORKSPACE
     assert kda.kda_resolve_algo(kda.KDA_BF16, 128, 128, 0, SPLIT) == SPLIT
     assert kda.kda_resolve_algo(kda.KDA_F32, 128, 128, 0, SPLIT) == -1
     assert kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=SPLIT) >= min_ws(2, 32)
@@ -208,3 +210,120 @@ def test_host_pipeline_matches_device(T, s0_std, final):
         np.testing.assert_array_equal(fs.numpy(), s_dev)
     o_ref, s_ref = ref(x)
     assert rel(out.float().numpy(), o_ref) <= 1e-2
+
+
+# ---- packed batches (cu_seqlens): chunk columns of every sequence at once --
+
+def run_packed(x, algo=SPLIT, status=None, workspace=True):
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    N = d["cu_seqlens"].numel() - 1
+    T, H = x["T"], x["H"]
+    out = torch.empty_like(d["v"])
+    fs = torch.empty(N, H, 128, 128, device="cuda")
+    ws, nb = None, 0
+    if workspace:
+        nb = kda.kda_workspace_bytes(N, T, H, 128, 128, algo=algo, packed=1)
+        ws = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda")
+    rc = kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"], out,
+                              fs, N, T, H, 128, 128, d["cu_seqlens"], kda.KDA_BF16, 0, 1.0, algo,
+                              ws, nb, status, torch.cuda.current_stream())
+    assert rc == 0, kda.status_string(rc)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), fs.cpu().numpy()
+
+
+@pytest.mark.parametrize("lens,s0_std", [((100, 64, 0, 1, 257, 130), 0.02),
+                                         ((640, 5, 63, 1000), 0.0),
+                                         ((1,), 0.03),
+                                         ((65, 0, 0, 128), 0.02)])
+def test_split_packed_matches_oracle(lens, s0_std):
+    """Sequences of every kind of length (empty, one token, partial and
+    whole chunks) packed in one batch: parity with the oracle, and the same
+    result as the fused kernel within the rounding of the shared operands."""
+    w = small_workload("pk", B=1, T=sum(lens), H=3, dk=128, dv=128, seed=41, varlen=True,
+                       lengths=lens, s0_std=s0_std)
+    x = make_inputs(w)
+    o, s = run_packed(x)
+    o_ref, s_ref = oracle.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["init_state"],
+                              x["cu_seqlens"])
+    assert rel(o, o_ref) <= 1e-2
+    assert rel(s, s_ref) <= 1e-2
+    o2, s2 = run_packed(x)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(s, s2)
+    of, sf = run_packed(x, algo=kda.KDA_ALGO_TC, workspace=False)
+    assert rel(o, of) <= 1e-2 and rel(s, sf) <= 1e-2
+
+
+def test_split_packed_bad_seqlens_reported():
+    lens = (100, 60, 96)
+    w = small_workload("pkb", B=1, T=256, H=2, dk=128, dv=128, seed=5, varlen=True,
+                       lengths=lens)
+    x = make_inputs(w)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x["cu_seqlens"] = torch.tensor([0, 100, 60, 256], dtype=torch.int32)  # not monotone
+    run_packed(x, status=status)
+    assert int(status.item()) == kda.KDA_ERR_BAD_SEQLENS
+    status.zero_()
+    x["cu_seqlens"] = torch.tensor([0, 100, 160, 250], dtype=torch.int32)  # ends before T
+    run_packed(x, status=status)
+    assert int(status.item()) == kda.KDA_ERR_BAD_SEQLENS
+
+
+def test_split_packed_checkpoints():
+    """Checkpoints of a packed batch on the two-kernel path equal the states
+    the oracle reaches at those positions of each sequence."""
+    lens = (200, 384, 64)
+    w = small_workload("pkc", B=1, T=sum(lens), H=2, dk=128, dv=128, seed=17, varlen=True,
+                       lengths=lens, s0_std=0.02)
+    x = make_inputs(w)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    N, T, H = 3, sum(lens), 2
+    out = torch.empty_like(d["v"])
+    fs = torch.empty(N, H, 128, 128, device="cuda")
+    ck = torch.full((N, H, 6, 128, 128), float("nan"), device="cuda")
+    assert kda.kda_resolve_path(N, T, H, packed=True) == SPLIT
+    rc = kda.kda_chunk_fwd_ckpt(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"], out,
+                                fs, N, T, H, 128, 128, d["cu_seqlens"], kda.KDA_BF16, 1.0, ck,
+                                128, 6, None, torch.cuda.current_stream())
+    assert rc == 0, kda.status_string(rc)
+    torch.cuda.synchronize()
+    ck = ck.cpu().numpy()
+    cu = x["cu_seqlens"].tolist()
+    for n in range(N):
+        for slot in range(6):
+            pos = 128 * (slot + 1)
+            if pos > lens[n]:
+                assert np.isnan(ck[n, :, slot]).all()
+                continue
+            sl = slice(cu[n], cu[n] + pos)
+            s0 = x["init_state"][n:n + 1]
+            _, s_ref = oracle.fwd(x["q"][:, sl], x["k"][:, sl], x["v"][:, sl], x["g"][:, sl],
+                                  x["beta"][:, sl], s0)
+            assert rel(ck[n, :, slot], s_ref[0]) <= 1e-2, (n, slot)
+
+
+def test_split_packed_first_call_in_a_process(tmp_path):
+    """A packed batch as the first two-kernel call of a process (nothing
+    before it has prepared the kernels' shared-memory limits)."""
+    import subprocess
+    import sys
+    import os
+    code = (
+        "import torch, numpy as np\n"
+        "from kda_inputs import small_workload, make_inputs\n"
+        "import gated_delta_rule_32_gb300 as pkg\n"
+        "from gated_delta_rule_32_gb300 import kda\n"
+        "kda.load()\n"
+        "w = small_workload('pk1', B=1, T=300, H=2, dk=128, dv=128, seed=3, varlen=True,"
+        " lengths=(100, 200))\n"
+        "x = make_inputs(w, device='cuda')\n"
+        "assert kda.kda_resolve_path(2, 300, 2, packed=True) == kda.KDA_ALGO_SPLIT\n"
+        "o, s = pkg.forward(x['q'], x['k'], x['v'], x['g'], x['beta'], None, x['cu_seqlens'])\n"
+        "torch.cuda.synchronize()\n"
+        "assert np.isfinite(o.float().cpu().numpy()).all()\n"
+        "print('ok')\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stderr[-2000:]
