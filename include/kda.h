@@ -80,13 +80,15 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
 /* Implementation choice for kda_chunk_fwd_ex (the result is the same
  * function of the inputs up to rounding). */
 typedef enum {
-  KDA_ALGO_AUTO = 0,  /* tensor-core path where built (two-kernel form for dense
-                       * batches, fused kernel for packed ones), else CUDA-core */
+  KDA_ALGO_AUTO = 0,  /* tensor-core path where built (two-kernel form; the fused
+                       * kernel for a packed batch whose chunk records would pass
+                       * 4 GiB), else CUDA-core */
   KDA_ALGO_SIMT = 1,  /* fp32 CUDA-core chunked path (16-token chunks) */
   KDA_ALGO_TC = 2,    /* tcgen05/TMEM/TMA fused path (bf16, dk = dv = 128) */
-  KDA_ALGO_SPLIT = 3  /* tensor-core path in two kernels (bf16, dk = dv = 128, dense
-                       * batches only): every chunk's state-independent part at once,
-                       * then the serial state pass; needs a workspace */
+  KDA_ALGO_SPLIT = 3  /* tensor-core path in two kernels (bf16, dk = dv = 128): every
+                       * chunk's state-independent part at once, then the serial
+                       * state pass; needs a workspace (packed batches: all
+                       * records at once) */
 } kda_algo;
 
 /* Human-readable name of a status code (static storage). */
@@ -121,10 +123,12 @@ kda_status kda_chunk_fwd_f32(const float* q, const float* k, const float* v,
  *               NULL: the library then takes it from the stream-ordered
  *               allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
  *               256-byte aligned.  The two-kernel path (KDA_ALGO_SPLIT)
- *               also accepts less, down to one chunk record per (sequence,
- *               head) plus the carried state (N * H * (82432 + 65536)
- *               bytes, rounded up to 256): it then runs the sequence in
- *               more, shorter slices; below that KDA_ERR_WORKSPACE.
+ *               also accepts less for a dense batch, down to one chunk
+ *               record per (sequence, head) plus the carried state
+ *               (N * H * (82432 + 65536) bytes, rounded up to 256): it then
+ *               runs the sequence in more, shorter slices; below that
+ *               KDA_ERR_WORKSPACE.  A packed batch needs the full size
+ *               (every chunk column, ceil(T / 64) + N at most, at once).
  *   dev_status  NULL or one device int32; set to KDA_OK at the start of the
  *               work and to a device-detected error if one occurs.
  */
