@@ -94,12 +94,11 @@ __device__ __forceinline__ void record_error(const kda::FwdParams& p, int* s_abo
   if (p.dev_status) atomicExch(p.dev_status, (int32_t)st);
 }
 
-
 // ===========================================================================
 // intra kernel
 // ===========================================================================
-// shared memory (bytes); 102 KiB so that two CTAs share an SM
-constexpr int I_Q = 0, I_K = 16384, I_G = 32768;  // TMA landing, 2 boxes of 64 channels each
+// shared memory (bytes); 110 KiB so that two CTAs share an SM
+constexpr int I_Q = 0, I_K = 16384, I_G = 32768;  // TMA landing, 2 unswizzled boxes of 64 channels
 constexpr int I_OB = 49152;                        // Gram operands for 64 key channels
 constexpr int I_A1 = I_OB;                         // [q0; k0; q1; k1] MN-major 128 x 64
 constexpr int I_B1 = I_OB + 16384;                 // [c0; c1]          MN-major  64 x 64
@@ -118,7 +117,7 @@ static_assert(I_T % 16 == 0, "T is an operand and a bulk-copy source");
 // first gate pass; the rest overlays what is dead by then
 constexpr int I_V = I_OB;                          // V landing, 2 boxes (until (beta V)^T)
 constexpr int I_AKK = I_OB, I_TF = I_OB + 18432;   // [64][72] fp32 each (after the Grams)
-constexpr int I_Y = I_Q + 8192;                    // Y fp32 [32][36]
+constexpr int I_Y = I_Q + 8192;                    // Y fp32 [32][36] (the solve, over dead Q)
 static_assert(I_V + 16384 <= I_BKG, "V landing");
 static_assert(I_TF + 64 * AKK_LD * 4 <= I_BKG, "solve scratch");
 static_assert(I_Y + 32 * 36 * 4 <= I_K, "block-merge scratch");
