@@ -122,9 +122,9 @@ static_assert(I_V + 16384 <= I_BKG, "V landing");
 static_assert(I_TF + 64 * AKK_LD * 4 <= I_BKG, "solve scratch");
 static_assert(I_Y + 32 * 36 * 4 <= I_K, "block-merge scratch");
 static_assert(2 * (I_SMEM + 1024) <= 233472, "two CTAs per SM");
-constexpr uint32_t I_TM_COLS = 128;
+constexpr uint32_t I_TM_COLS = 256;
 constexpr uint32_t TM_G = 0;     // Gram products: [0, 64) diagonal halves, [64, 96) cross
-constexpr uint32_t TM_W = 0;     // W^T (after the Grams are read)
+constexpr uint32_t TM_W = 128;   // W^T, read out while the next item's Grams are formed
 
 __global__ void __launch_bounds__(kThreads, 2)
     kda_tc_intra_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -366,14 +366,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       g_issued = li + 2;
       beta_raw = load_beta(nxt);
     }
-    // the previous item's W product, then its rows into that record; its T
-    // copy has left shared memory before this item's solve rewrites it
-    // (a thread that saw the wait fail skips the rows; the loop leaves at
-    // the next check that follows a barrier)
+    // the previous item's W product (its rows go out during this item's
+    // first Gram product); its T copy has left shared memory before this
+    // item's solve rewrites it (a thread that saw the wait fail skips the
+    // rows; the loop leaves at the next check that follows a barrier)
     if (w_rec) {
       wait_mma();
-      if (!*s_abort) w_out(w_rec);
-      w_rec = nullptr;
       if (tid == 32) sm100::bulk_wait_read();
     }
     // (beta V)^T, K-major [value channel jv][row r], into the record; V is
@@ -547,6 +545,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     sync_all();
     SPLIT_MARK(3, mk);
     gram_mma(0);
+    // the previous item's W rows, while the tensor cores form the Grams
+    // (W has its own tensor-memory columns)
+    if (w_rec) {
+      if (!*s_abort) w_out(w_rec);
+      w_rec = nullptr;
+    }
     wait_mma();
     SPLIT_MARK(4, mk);
     gate_pass(al1, 1);
