@@ -88,6 +88,26 @@ def test_staging_bytes(lib):
     assert n >= 3 * qk + 2 * 2 * 100 * 3 * 64 * 2 + 2 * 2 * 3 * 128 * 64 * 4
 
 
+def test_staging_bytes_of_the_pipelined_host_call(lib):
+    # dense bf16 at dk = dv = 128 runs the end-to-end call in up to eight
+    # pieces of whole chunks: the staging holds the inputs, outputs and
+    # states plus the chunk records of one piece (64 of the 512 chunks here)
+    def r256(x):
+        return (x + 255) // 256 * 256
+    B, T, H = 2, 32768, 32
+    qk = B * T * H * 128 * 2
+    state = B * H * 128 * 128 * 4
+    fixed = 3 * r256(qk) + 2 * r256(qk) + r256(B * T * H * 2) + 2 * r256(state) + 256
+    piece = r256(state) + B * H * 82432 * 64
+    n = kda.kda_host_staging_bytes(B, T, H, 128, 128, kda.KDA_BF16, 1, 1, 0)
+    assert n == fixed + r256(piece)
+    # a single chunk is not cut: the whole-call workspace
+    n1 = kda.kda_host_staging_bytes(B, 64, H, 128, 128, kda.KDA_BF16, 0, 1, 0)
+    qk1 = B * 64 * H * 128 * 2
+    assert n1 == 5 * r256(qk1) + r256(B * 64 * H * 2) + r256(state) + 256 + \
+        r256(kda.kda_workspace_bytes(B, 64, H, 128, 128))
+
+
 def test_package_fails_loudly_without_library(tmp_path):
     saved = kda._lib
     try:
