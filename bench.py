@@ -43,6 +43,31 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_workload(base, rank: int):
+    """Rank r's batch: the same workload, its units drawn as rows r B ..
+    r B + B - 1 of one long batch (and seed + 1000 r), so that the ranks run
+    independent batches; rank 0 keeps the base workload."""
+    import dataclasses
+    if not rank:
+        return base
+    return dataclasses.replace(base, seed=base.seed + 1000 * rank,
+                               row_offset=base.row_offset + rank * base.B)
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """The largest x over the ranks (x itself on one rank)."""
+    if ws <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ws: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's step."""
+    return ws * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def alg_bytes(w, has_init: bool, has_final: bool) -> int:
     """Algorithmic HBM bytes of one forward: every input read once, every
     output written once (bf16 q, k, g, v, beta, out; fp32 states)."""
@@ -250,8 +275,7 @@ def run_ours(args):
     kda.load()
 
     base = resolve_workload(args)
-    import dataclasses
-    w = dataclasses.replace(base, seed=base.seed + 1000 * rank) if rank else base
+    w = rank_workload(base, rank)
     x = make_inputs(w)
     d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
     N, T, H, dk, dv = x["B"], x["T"], x["H"], x["dk"], x["dv"]
@@ -298,15 +322,11 @@ def run_ours(args):
     if ws > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), ws, dev)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     tokens = w.B * w.T
-    value = ws * tokens / (ms_per_step / 1e3)
+    value = job_value(ws, tokens, ms_per_step)
 
     # ---- the two kernels of the split path, each timed alone ----------------
     path = kda.kda_resolve_path(N, T, H, dk, dv, dtype, 0, args.algo, w.varlen)
@@ -362,16 +382,12 @@ def run_ours(args):
         t0 = time.perf_counter()
         for _ in range(n_e2e):
             host_step()
-        e2e_s = (time.perf_counter() - t0) / n_e2e
-        if ws > 1:
-            t = torch.tensor([e2e_s], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_s = float(t.item())
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, ws, dev)
         h2d = sum(pin[k].numel() * pin[k].element_size()
                   for k in ("q", "k", "v", "g", "beta", "init_state", "cu_seqlens")
                   if pin[k] is not None)
         d2h = hout.numel() * hout.element_size() + hfs.numel() * 4 + 4
-        e2e = {"value": ws * tokens / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_value(ws, tokens, e2e_s * 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e}
 
     if ws > 1 and rank != 0:

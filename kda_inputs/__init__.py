@@ -52,6 +52,9 @@ class Workload:
     lengths: Optional[tuple] = None  # explicit varlen lengths (else drawn)
     varlen_lo: int = 128
     varlen_hi: int = 4096
+    # added to the batch row of every unit's stream: ranks of a multi-GPU
+    # run draw rows r*B .. r*B+B-1 of one long batch, so their data differ
+    row_offset: int = 0
 
     @property
     def tokens(self) -> int:
@@ -128,7 +131,7 @@ def make_unit(w: Workload, b: int, h: int):
     Returns dict q [T,dk], k [T,dk], v [T,dv], beta [T], g [T,dk] and s0
     [n_seq_in_row, dk, dv] (zeros when the workload has a zero state).
     """
-    g = torch.Generator().manual_seed(unit_seed(w.seed, b, h))
+    g = torch.Generator().manual_seed(unit_seed(w.seed, b + w.row_offset, h))
     T = w.T
     q = torch.randn(T, w.dk, generator=g)
     k = torch.randn(T, w.dk, generator=g)
