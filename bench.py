@@ -142,7 +142,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -298,6 +298,22 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    if not args.steps:
+        # no count given: enough steps for a timed region of about 1.2 s, so
+        # that the clock sampler sees several readings under load
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(3):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        est = max(e0.elapsed_time(e1) / 3, 1e-3)
+        n = int(min(5000, max(20, 1200.0 / est)))
+        if ws > 1:   # every rank times the same count
+            t = torch.tensor([n], dtype=torch.int64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            n = int(t.item())
+        args.steps = n
 
     # ---- device-timed region: K steps, inputs resident in HBM --------------
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
@@ -348,7 +364,7 @@ def run_ours(args):
                                        d["init_state"], out, fs, N, T, H, 1.0, swork, sws,
                                        None, stream)
         if one_slice and stage(1) == 0 and stage(2) == 0:
-            n_k = max(3, args.steps)
+            n_k = max(3, min(args.steps, 50))
             for sg, name in ((1, "kda_tc_intra_kernel"), (2, "kda_tc_state_kernel")):
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
@@ -451,7 +467,8 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (default: as many as fill about 1.2 s)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
@@ -470,6 +487,8 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
+        if not args.steps:
+            args.steps = 5
         return run_reference(args)
     return run_ours(args)
 

@@ -4,7 +4,44 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "kda_common.cuh"
+
+namespace {
+std::mutex g_dev_mu;
+std::map<std::pair<int, const void*>, int> g_smem_set;  // (device, kernel) -> bytes set
+std::map<int, int> g_sms;                                // device -> SM count
+}  // namespace
+
+kda_status kda_smem_attr(const void* func, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  auto key = std::make_pair(dev, func);
+  auto it = g_smem_set.find(key);
+  if (it != g_smem_set.end() && it->second >= bytes) return KDA_OK;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return KDA_ERR_CUDA;
+  g_smem_set[key] = bytes;
+  return KDA_OK;
+}
+
+int kda_device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  auto it = g_sms.find(dev);
+  if (it != g_sms.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 0;
+  g_sms[dev] = n;
+  return n;
+}
 
 size_t kda_split_packed_workspace_bytes(int N, int T, int H);
 
@@ -65,14 +102,8 @@ kda_status check_args(const void* q, const void* k, const void* v, const void* g
 }
 
 int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      n = 148;
-  }
-  return n;
+  const int n = kda_device_sms();
+  return n > 0 ? n : 148;
 }
 
 // Segments per sequence for the tensor-core path: only dense batches whose
@@ -112,6 +143,14 @@ bool use_split(int dtype, int dk, int dv, int chunk_size, int algo, int packed, 
 }
 
 }  // namespace
+
+kda_status kda_check_args(const void* q, const void* k, const void* v, const void* g,
+                          const void* beta, const float* s0, const void* out, const float* s1,
+                          int B, int T, int H, int dk, int dv, const int32_t* cu, int dtype,
+                          int chunk_size, int algo) {
+  return check_args(q, k, v, g, beta, s0, out, s1, B, T, H, dk, dv, cu, dtype, chunk_size,
+                    algo);
+}
 
 kda_status kda_run_segmented(const kda::FwdParams& p, int nseg, void* scratch,
                              cudaStream_t stream);

@@ -87,6 +87,23 @@ __device__ __forceinline__ bool seq_span(const FwdParams& p, int n, int64_t& row
 
 }  // namespace kda
 
+// Per-device launch set-up, kept per (device, kernel) for the life of the
+// process and safe to call from several host threads at once (kda_api.cu).
+// kda_smem_attr raises kernel `func`'s dynamic shared-memory limit to
+// `bytes` on the current device, the first time that pair is seen;
+// kda_device_sms returns the current device's SM count (0 if the runtime
+// cannot tell).
+kda_status kda_smem_attr(const void* func, int bytes);
+int kda_device_sms();
+
+// The argument rules of the C ABI (kda_api.cu): sizes, NULL pointers,
+// alignment, the supported dk / dv / chunk / dtype, and no overlap of the
+// output (or of a final state other than the initial one) with any input.
+kda_status kda_check_args(const void* q, const void* k, const void* v, const void* g,
+                          const void* beta, const float* s0, const void* out, const float* s1,
+                          int B, int T, int H, int dk, int dv, const int32_t* cu, int dtype,
+                          int chunk_size, int algo);
+
 // Launchers (one per translation unit).
 kda_status kda_launch_simt(const kda::FwdParams& p, kda_dtype dtype, cudaStream_t stream);
 kda_status kda_launch_tc(const kda::FwdParams& p, cudaStream_t stream);

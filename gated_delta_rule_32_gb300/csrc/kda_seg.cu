@@ -63,13 +63,7 @@ __global__ void __launch_bounds__(256) kda_seg_scan_kernel(kda::FwdParams p) {
 
 kda_status kda_launch_seg_scan(const kda::FwdParams& p, cudaStream_t stream) {
   const size_t smem = sizeof(float) * (DK * LDP + DK * SC);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kda_seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return KDA_ERR_CUDA;
-    attr_set = true;
-  }
+  if (kda_smem_attr((const void*)kda_seg_scan_kernel, (int)smem) != KDA_OK) return KDA_ERR_CUDA;
   dim3 grid(p.H, p.N, p.dv / SC);
   kda_seg_scan_kernel<<<grid, 256, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;

@@ -52,25 +52,29 @@ extern "C" kda_status kda_chunk_fwd_seg_static(const uint16_t* q, const uint16_t
                                                uint16_t* out, float* final_state, int B, int T,
                                                int H, int dk, int dv, float scale, int nseg,
                                                int32_t* dev_status, kda_stream_t stream_) {
-  if (B < 1 || T < 0 || H < 1) return KDA_ERR_INVALID_ARG;
-  if (T > 0 && (!q || !k || !v || !g_logit || !beta || !out)) return KDA_ERR_INVALID_ARG;
+  // the same argument rules as kda_chunk_fwd_seg
+  kda_status st = kda_check_args(q, k, v, g_logit, beta, init_state, out, final_state, B, T, H,
+                                 dk, dv, nullptr, KDA_BF16, 0, KDA_ALGO_TC);
+  if (st != KDA_OK) return st;
   if (!kda_tc_supported(dk, dv)) return KDA_ERR_UNSUPPORTED;
   if (nseg < 2 || nseg > 4096) return KDA_ERR_INVALID_ARG;
-  const uintptr_t pq = (uintptr_t)q | (uintptr_t)k | (uintptr_t)v | (uintptr_t)g_logit |
-                       (uintptr_t)out | (uintptr_t)init_state | (uintptr_t)final_state;
-  if ((pq & 15) != 0 || ((uintptr_t)beta & 1) != 0) return KDA_ERR_MISALIGNED;
   // everything beyond the fixed array is refused before anything is queued
   if (kda_seg_scratch_bytes(B, H, nseg, dk, dv) > kStaticScratchBytes) return KDA_ERR_WORKSPACE;
-  void* scratch = nullptr;
-  kda_status st = scratch_address(&scratch);
-  if (st != KDA_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), stream) != cudaSuccess)
-    return KDA_ERR_CUDA;
   kda::FwdParams p{};
   p.q = q; p.k = k; p.v = v; p.g = g_logit; p.beta = beta;
   p.init_state = init_state; p.out = out; p.final_state = final_state;
   p.dev_status = dev_status;
   p.N = B; p.T = T; p.H = H; p.dk = dk; p.dv = dv; p.scale = scale;
+  if (T == 0) {  // no tokens: the states pass through, as in kda_chunk_fwd_seg
+    if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), stream) != cudaSuccess)
+      return KDA_ERR_CUDA;
+    return kda_launch_tc(p, stream);
+  }
+  void* scratch = nullptr;
+  st = scratch_address(&scratch);
+  if (st != KDA_OK) return st;
+  if (dev_status && cudaMemsetAsync(dev_status, 0, sizeof(int32_t), stream) != cudaSuccess)
+    return KDA_ERR_CUDA;
   return kda_run_segmented(p, nseg, scratch, stream);
 }

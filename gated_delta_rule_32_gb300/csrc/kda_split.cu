@@ -1217,24 +1217,15 @@ kda_status plan_split(const kda::FwdParams& p, void* workspace, size_t workspace
     pl.nchunks = (int)(((int64_t)p.T + C - 1) / C);
     pl.fit = (workspace_bytes - pl.carry) / pl.per;
   }
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&pl.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      pl.sms < 1)
-    return KDA_ERR_CUDA;
+  pl.sms = kda_device_sms();
+  if (pl.sms < 1) return KDA_ERR_CUDA;
   // unswizzled tiles: every read of them goes along one row
   if (!make_map(&pl.mq, p.q, rows, p.H, DK, false) || !make_map(&pl.mk, p.k, rows, p.H, DK, false) ||
       !make_map(&pl.mg, p.g, rows, p.H, DK, false) || !make_map(&pl.mv, p.v, rows, p.H, DV, false))
     return KDA_ERR_CUDA;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kda_tc_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             I_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(kda_tc_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             S_SMEM) != cudaSuccess)
-      return KDA_ERR_CUDA;
-    attr_set = true;
-  }
+  if (kda_smem_attr((const void*)kda_tc_intra_kernel, I_SMEM) != KDA_OK ||
+      kda_smem_attr((const void*)kda_tc_state_kernel, S_SMEM) != KDA_OK)
+    return KDA_ERR_CUDA;
   if (pl.packed) {
     pl.rec = static_cast<unsigned char*>(workspace) + packed_layout(p.N, p.T, p.H).rec_at;
     pl.through = nullptr;

@@ -862,14 +862,9 @@ kda_status launch_tc(const TcParams& tp, cudaStream_t stream) {
     memset(&mq, 0, sizeof(mq));
     mk = mq; mg = mq; mv = mq;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kda_tc_fused_kernel<MODE, DBG>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Lay<MODE>::SMEM_BYTES) != cudaSuccess)
-      return KDA_ERR_CUDA;
-    attr_set = true;
-  }
+  if (kda_smem_attr((const void*)kda_tc_fused_kernel<MODE, DBG>, Lay<MODE>::SMEM_BYTES) !=
+      KDA_OK)
+    return KDA_ERR_CUDA;
   dim3 grid(2, p.H, p.N * nseg);
   kda_tc_fused_kernel<MODE, DBG><<<grid, kThreads, Lay<MODE>::SMEM_BYTES, stream>>>(mq, mk, mg, mv, tp);
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;

@@ -206,7 +206,10 @@ kda_status kda_chunk_fwd_seg(const uint16_t* q, const uint16_t* k, const uint16_
  * 128) are refused with KDA_ERR_WORKSPACE before anything is queued.  The
  * caller still provides inputs and outputs.  The first call on a device
  * looks up the array's device address (a runtime query, no allocation);
- * make that first call before any stream capture.  All calls share the one
+ * make that first call before any stream capture.  The address is kept for
+ * the life of the process, so do not use this entry point on a device after
+ * cudaDeviceReset() there (the array then lives at a new address).  The
+ * argument rules are those of kda_chunk_fwd_seg.  All calls share the one
  * array and nothing in it needs to start at zero (every value read was
  * written earlier in the same call), so calls that overlap on the GPU race:
  * issue them on one stream, or otherwise one at a time.

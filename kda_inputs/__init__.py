@@ -97,8 +97,30 @@ def small_workload(name: str, **kw) -> Workload:
     return Workload(name, **base)
 
 
+_MASK64 = (1 << 64) - 1
+
+
+def _splitmix64(x: int) -> int:
+    """One step of the splitmix64 generator (Steele, Lea and Flood, "Fast
+    splittable pseudorandom number generators", OOPSLA 2014): a bijective
+    64-bit mix in which every input bit reaches every output bit."""
+    x = (x + 0x9E3779B97F4A7C15) & _MASK64
+    x = ((x ^ (x >> 30)) * 0xBF58476D1CE4E5B9) & _MASK64
+    x = ((x ^ (x >> 27)) * 0x94D049BB133111EB) & _MASK64
+    return x ^ (x >> 31)
+
+
 def unit_seed(seed: int, b: int, h: int) -> int:
-    return (seed << 32) + (b << 16) + h
+    """Seed of the (batch row b, head h) stream of a workload seeded ``seed``.
+
+    torch's CPU generator keeps only the low 32 bits of a seed, so the three
+    numbers are chained through splitmix64 and the result is cut to 32 bits:
+    every workload seed, row and head reaches the bits the generator uses.
+    """
+    x = _splitmix64(seed & _MASK64)
+    x = _splitmix64(x ^ (b & _MASK64))
+    x = _splitmix64(x ^ (h & _MASK64))
+    return x & 0xFFFFFFFF
 
 
 def varlen_lengths(total: int, seed: int, lo: int = 128, hi: int = 4096) -> list:

@@ -178,3 +178,35 @@ def p10_split(fwd_unit, seed=20, T=150, dk=8, dv=6, cuts=(64, 77)):
 
 ALL = [p1_retrieval, p2_beta_zero, p3_deltanet, p4_orthonormal_keys, p5_repeated_key,
        p6_small_beta, p8_affine, p10_split]
+
+
+def p11_scale(fwd_scaled, seed=21, T=18, dk=6, dv=5, s=0.37):
+    """The q scale multiplies the read-out only: o_t = S_t^T (s q_t).  Checked
+    against two routes that do not use the implementation's unscaled run:
+    (a) DeltaNet (alpha = 1) by explicit dk x dk transition matrices, read out
+    with s q_t; (b) the retrieval identity with beta = 1 and q = k, which gives
+    o_t = s v_t.  The final state must not depend on s at all."""
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((T, dk)); k = _unit(rng, T, dk)
+    v = rng.standard_normal((T, dv)); beta = rng.uniform(0, 1, T)
+    g = np.full((T, dk), -200.0); s0 = rng.standard_normal((dk, dv))
+    S = s0.copy(); ref = np.zeros((T, dv))
+    for t in range(T):
+        A = np.eye(dk) - beta[t] * np.outer(k[t], k[t])
+        S = A @ S + beta[t] * np.outer(k[t], v[t])
+        ref[t] = S.T @ (s * q[t])
+    o, ST = fwd_scaled(q, k, v, g, beta, s0, s)
+    e1 = max(_rel(o, ref), _rel(ST, S))
+    # retrieval: beta = 1 and q = k at the probe steps, any gates
+    g2 = rng.standard_normal((T, dk)) * 2
+    beta2 = rng.uniform(0.05, 0.95, T)
+    q2 = q.copy()
+    probe = np.arange(2, T, 4)
+    beta2[probe] = 1.0
+    q2[probe] = k[probe]
+    o2, S2 = fwd_scaled(q2, k, v, g2, beta2, s0, s)
+    e2 = _rel(o2[probe], s * v[probe])
+    _, S2u = fwd_scaled(q2, k, v, g2, beta2, s0, 1.0)
+    e3 = _rel(S2, S2u)
+    err = max(e1, e2, e3)
+    return err < 1e-12, err

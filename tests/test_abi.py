@@ -157,3 +157,25 @@ def test_resolve_path(lib):
     assert rp(2, 100, 4, dk=64) == kda.KDA_ALGO_SIMT
     assert rp(0, 100, 4) == -1
     assert rp(2, 100, 4, dtype=kda.KDA_F32, algo=kda.KDA_ALGO_SPLIT) == -1
+
+
+def test_allocation_free_entry_has_the_same_argument_rules(lib):
+    # kda_chunk_fwd_seg_static refuses exactly what kda_chunk_fwd_seg refuses,
+    # before anything is queued (fake addresses, never dereferenced)
+    def st(**over):
+        a = dict(q=A, k=2 * A, v=3 * A, g_logit=4 * A, beta=5 * A, init_state=None,
+                 out=6 * A, final_state=None, B=1, T=256, H=2, dk=128, dv=128, scale=1.0,
+                 nseg=2)
+        a.update(over)
+        return kda.kda_chunk_fwd_seg_static(**a)
+    assert st(out=A) == kda.KDA_ERR_INVALID_ARG              # out == q
+    assert st(out=3 * A + 64) == kda.KDA_ERR_INVALID_ARG     # out overlaps v
+    assert st(final_state=2 * A) == kda.KDA_ERR_INVALID_ARG  # final state over k
+    assert st(init_state=6 * A) == kda.KDA_ERR_INVALID_ARG   # initial state under out
+    assert st(q=None) == kda.KDA_ERR_INVALID_ARG
+    assert st(q=A + 8) == kda.KDA_ERR_MISALIGNED
+    assert st(init_state=7 * A + 4) == kda.KDA_ERR_MISALIGNED
+    assert st(dk=64) == kda.KDA_ERR_UNSUPPORTED
+    assert st(nseg=1) == kda.KDA_ERR_INVALID_ARG
+    # past the fixed scratch array: refused before any device work
+    assert st(H=32, nseg=8) == kda.KDA_ERR_WORKSPACE

@@ -26,16 +26,20 @@ def rel(a, b):
 
 @pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, 1e-2), (torch.float32, 1e-4)])
 @pytest.mark.parametrize("T", [1, 3, 8])
-@pytest.mark.parametrize("d", [64, 128])
-def test_decode_matches_oracle(dtype, tol, T, d):
-    w = small_workload("dec", B=3, T=T, H=4, dk=d, dv=d, dtype=dtype, s0_std=0.5, seed=T * d)
+@pytest.mark.parametrize("dk,dv", [(16, 16), (32, 32), (64, 64), (128, 128), (32, 64),
+                                   (128, 16)])
+def test_decode_matches_oracle(dtype, tol, T, dk, dv):
+    # every head size the entry point accepts: dk = 16 leaves two key rows per
+    # warp, dv = 16 half of a CTA's 32 value lanes idle
+    w = small_workload("dec", B=3, T=T, H=4, dk=dk, dv=dv, dtype=dtype, s0_std=0.5,
+                       seed=T * dk + dv)
     x = make_inputs(w)
     dev = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
     st = dev["init_state"].clone()
     out = torch.empty_like(dev["v"])
     dt = kda.KDA_BF16 if dtype == torch.bfloat16 else kda.KDA_F32
     rc = kda.kda_decode(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], st, out, 3, T, 4,
-                        d, d, dt, 1.0, torch.cuda.current_stream())
+                        dk, dv, dt, 1.0, torch.cuda.current_stream())
     assert rc == 0
     torch.cuda.synchronize()
     o_ref, s_ref = oracle.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["init_state"])

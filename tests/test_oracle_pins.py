@@ -313,3 +313,75 @@ def test_pins_reject_mutant(name):
 def test_floor_pin_on_oracle():
     assert _floor_pin(c_unit)
     assert _floor_pin(mirror_unit(4))
+
+
+# ---- the q scale -------------------------------------------------------------
+
+def _c_scaled(q, k, v, g, beta, s0, scale):
+    return oracle.fwd_unit(q, k, v, g, beta, s0, scale=scale)
+
+
+def _mirror_scaled(C):
+    def f(q, k, v, g, beta, s0, scale):
+        return chunk_mirror.forward_unit(q, k, v, g, beta, s0, chunk=C, scale=scale)
+    return f
+
+
+def test_scale_pin_c_oracle():
+    ok, err = _pins.p11_scale(_c_scaled)
+    assert ok, err
+
+
+@pytest.mark.parametrize("C", [1, 16, 64])
+def test_scale_pin_chunk_mirror(C):
+    ok, err = _pins.p11_scale(_mirror_scaled(C))
+    assert ok, (C, err)
+
+
+def test_scale_batched_oracle_is_linear_in_scale():
+    # the batched entry (several heads, packed sequences) scales o only
+    rng = np.random.default_rng(31)
+    lens = [9, 40, 23]
+    Tt, H, dk, dv = sum(lens), 2, 8, 4
+    q = rng.standard_normal((1, Tt, H, dk)); k = rng.standard_normal((1, Tt, H, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((1, Tt, H, dv)); g = rng.standard_normal((1, Tt, H, dk))
+    beta = rng.uniform(0, 1, (1, Tt, H)); s0 = rng.standard_normal((len(lens), H, dk, dv))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    o1, S1 = oracle.fwd(q, k, v, g, beta, s0, cu_seqlens=cu)
+    o2, S2 = oracle.fwd(q, k, v, g, beta, s0, cu_seqlens=cu, scale=-2.5)
+    np.testing.assert_allclose(o2, -2.5 * o1, rtol=1e-14, atol=1e-14 * np.abs(o1).max())
+    np.testing.assert_array_equal(S2, S1)
+    o3, S3 = chunk_mirror.forward(q, k, v, g, beta, s0, cu_seqlens=cu, scale=-2.5)
+    np.testing.assert_allclose(o3, o2, rtol=0, atol=1e-10 * np.abs(o2).max())
+    np.testing.assert_allclose(S3, S2, rtol=0, atol=1e-10 * np.abs(S2).max())
+
+
+def _scale_mutant(kind):
+    base = _mutant("none")
+
+    def f(q, k, v, g, beta, s0, scale):
+        q, k, v = (np.asarray(t, dtype=np.float64) for t in (q, k, v))
+        if kind == "scale_on_k":
+            return base(q, k * scale, v, g, beta, s0)
+        if kind == "scale_on_v":
+            return base(q, k, v * scale, g, beta, s0)
+        if kind == "scale_on_state":
+            o, S = base(q, k, v, g, beta, s0)
+            return o * scale, S * scale
+        if kind == "scale_squared":
+            return base(q * scale * scale, k, v, g, beta, s0)
+        return base(q * scale, k, v, g, beta, s0)
+    return f
+
+
+def test_scale_pin_accepts_reference_loop():
+    ok, err = _pins.p11_scale(_scale_mutant("none"))
+    assert ok, err
+
+
+@pytest.mark.parametrize("kind", ["scale_on_k", "scale_on_v", "scale_on_state",
+                                  "scale_squared"])
+def test_scale_pin_rejects_mutant(kind):
+    ok, _ = _pins.p11_scale(_scale_mutant(kind))
+    assert not ok, kind
