@@ -350,7 +350,7 @@ def run_ours(args):
     launches_per_step = 1
     split_ms = {}
     if split:
-        rec = 82432  # bytes of one chunk record
+        rec = 66048  # bytes of one chunk record
         sws = ws_bytes
         carry = (N * H * dk * dv * 4 + 255) // 256 * 256
         nchunks = (T + 63) // 64

@@ -2,7 +2,8 @@
 //
 // Everything of a chunk that does not depend on the state entering it (the
 // gate, the Gram matrices, T = (I + beta A_kk)^{-1}, W = T (beta K gamma),
-// U = T (beta V), Q gamma and K e^{G_C - G}) is independent across chunks;
+// U = T (beta V) = (T Diag(beta)) V, Q gamma and K e^{G_C - G}) is
+// independent across chunks;
 // only Delta = U - W S, O = (Q gamma) S + A_qk Delta and
 // S <- gamma_C S + (K dec)^T Delta chain one chunk to the next (Towards AI
 // walkthrough, "Infrastructure co-design": the chunk-to-chunk state
@@ -11,15 +12,16 @@
 //                 chunk) items; writes one record per chunk to global
 //                 memory, laid out as the state kernel's shared-memory image;
 //   state kernel  one CTA per (half of the value channels, head, sequence);
-//                 per chunk a bulk copy of the record, the U product of its
+//                 per chunk a bulk copy of the record and a TMA load of its
+//                 half of V straight from the input, the U product of its
 //                 half (off the chain: it runs while the CUDA cores copy the
 //                 state), then two tensor-core products and two short
 //                 epilogues on the chain, the state in tensor memory
 //                 throughout.
-// The record holds the operands in the precision the fused kernel feeds its
-// own products (bf16 W, Q gamma, K dec, A_qk, T, beta V; fp32 gamma_C), and
-// U is accumulated in fp32 from the same bf16 T and beta V, so the two paths
-// round at the same points.
+// The record holds bf16 operands (W, Q gamma, K dec, A_qk, T Diag(beta)) and
+// fp32 gamma_C; U is accumulated in fp32 from the bf16 T Diag(beta) and the
+// input's own bf16 V, so V is never rewritten and the record carries nothing
+// of the size of V.
 //
 // A long sequence runs in slices of chunks (intra kernel over the slice,
 // then the state kernel over it), so the record buffer stays bounded; the
@@ -43,18 +45,22 @@ constexpr int AKK_LD = 72;
 constexpr int REC_KD = 0;        // (K dec)^T, K-major [key channel j][row r]  16384
 constexpr int REC_AQ = 16384;    // A_qk masked (i <= r), K-major [r][i]         8192
 constexpr int REC_WQ = 24576;    // [W; Q gamma], MN-major 128 rows x 128 K     32768
-constexpr int REC_T = 57344;     // T = (I + beta A_kk)^-1, K-major [r][i]       8192
-constexpr int REC_BV = 65536;    // (beta V)^T, K-major [value channel][r]      16384
-constexpr int REC_GC = 81920;    // gamma_C fp32 [128]                             512
-constexpr int REC_BYTES = 82432;
-// the part of a record one state CTA copies: KD | AQ | WQ | T, the (beta V)^T
-// rows of its value half, gamma_C.  U = T (beta V) of the half is formed
-// there, on the tensor cores, into tensor memory: its rows past 63 read the
-// (beta V)^T rows that follow T and are never used.
-constexpr int ST_KD = 0, ST_AQ = 16384, ST_WQ = 24576, ST_T = 57344, ST_BV = 65536,
+constexpr int REC_T = 57344;     // T Diag(beta), K-major [r][i]                  8192
+constexpr int REC_GC = 65536;    // gamma_C fp32 [128]                             512
+constexpr int REC_BYTES = 66048;
+// what one state CTA holds per chunk: the record (KD | AQ | WQ | T Diag(beta)
+// by one bulk copy, gamma_C by another) and the 64 value channels of its half
+// of V, loaded from the input by TMA in 8-channel boxes, each box 64 rows x
+// 16 bytes: together an MN-major operand (N = value channel, K = row; K
+// groups 128 B apart, N groups 1024 B apart).  U = T Diag(beta) V of the half
+// is formed there, on the tensor cores, into tensor memory: its rows past 63
+// read the V tile that follows T and are never used.
+constexpr int ST_KD = 0, ST_AQ = 16384, ST_WQ = 24576, ST_T = 57344, ST_V = 65536,
               ST_GC = 73728;
 constexpr int STAGE_BYTES = 74240;
-static_assert(ST_BV == ST_T + 8192 && REC_BV == REC_T + 8192, "U operand rows");
+constexpr int ST_COPY = REC_GC;  // bytes of the record's first bulk copy
+static_assert(ST_V == ST_T + 8192, "U operand rows");
+static_assert(ST_COPY == ST_V, "first bulk copy ends where V starts");
 
 struct SplitParams {
   kda::FwdParams p;
@@ -104,8 +110,8 @@ constexpr int I_A1 = I_OB;                         // [q0; k0; q1; k1] MN-major 
 constexpr int I_B1 = I_OB + 16384;                 // [c0; c1]          MN-major  64 x 64
 constexpr int I_A2 = I_OB + 24576;                 // [q1'; k1']        MN-major  64 x 64
 constexpr int I_B2 = I_OB + 32768;                 // c0'               MN-major  32 x 64
-constexpr int I_BKG = I_OB + 36864;                // (beta K gamma)^T K-major 128 x 64
-constexpr int I_BETA = I_BKG + 16384;              // 64 raw bf16
+constexpr int I_KG = I_OB + 36864;                 // (K gamma)^T K-major 128 x 64
+constexpr int I_BETA = I_KG + 16384;               // 64 raw bf16
 constexpr int I_PT = I_BETA + 128;                 // [4 tiles][128] fp32 tile products
 static_assert(I_BETA % 16 == 0, "beta rows are read 8 at a time");
 constexpr int I_BAR = I_PT + 2048;
@@ -113,13 +119,10 @@ constexpr int I_MISC = I_BAR + 64;
 constexpr int I_T = I_MISC + 64;                   // T bf16 K-major [r][i] (8192)
 constexpr int I_SMEM = I_T + 8192;
 static_assert(I_T % 16 == 0, "T is an operand and a bulk-copy source");
-// V lands with Q, K, G in the Gram operand buffer, which is free until the
-// first gate pass; the rest overlays what is dead by then
-constexpr int I_V = I_OB;                          // V landing, 2 boxes (until (beta V)^T)
+// the solve's scratch overlays what is dead by then
 constexpr int I_AKK = I_OB, I_TF = I_OB + 18432;   // [64][72] fp32 each (after the Grams)
 constexpr int I_Y = I_Q + 8192;                    // Y fp32 [32][36] (the solve, over dead Q)
-static_assert(I_V + 16384 <= I_BKG, "V landing");
-static_assert(I_TF + 64 * AKK_LD * 4 <= I_BKG, "solve scratch");
+static_assert(I_TF + 64 * AKK_LD * 4 <= I_KG, "solve scratch");
 static_assert(I_Y + 32 * 36 * 4 <= I_K, "block-merge scratch");
 static_assert(2 * (I_SMEM + 1024) <= 233472, "two CTAs per SM");
 constexpr uint32_t I_TM_COLS = 256;
@@ -129,8 +132,7 @@ constexpr uint32_t TM_W = 128;   // W^T, read out while the next item's Grams ar
 __global__ void __launch_bounds__(kThreads, 2)
     kda_tc_intra_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_g,
-                        const __grid_constant__ CUtensorMap tm_v, const SplitParams sp) {
+                        const __grid_constant__ CUtensorMap tm_g, const SplitParams sp) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const kda::FwdParams& p = sp.p;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -213,8 +215,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* bar_q = reinterpret_cast<uint64_t*>(smem + I_BAR);  // Q tiles
   uint64_t* bar_g = bar_q + 1;                                   // decay-logit tiles
   uint64_t* bar_k = bar_q + 2;                                   // K tiles
-  uint64_t* bar_v = bar_q + 3;                                   // V tiles
-  uint64_t* bar_mma = bar_q + 4;
+  uint64_t* bar_mma = bar_q + 3;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + I_MISC);
   int* s_abort = reinterpret_cast<int*>(smem + I_MISC + 4);
   unsigned short* s_beta_raw = reinterpret_cast<unsigned short*>(smem + I_BETA);
@@ -242,11 +243,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     sm100::tma_load_3d(smem + I_K, &tm_k, bar_k, 0, it.h, (int)it.row0);
     sm100::tma_load_3d(smem + I_K + 8192, &tm_k, bar_k, 64, it.h, (int)it.row0);
   };
-  auto load_v = [&](const Item& it) {
-    sm100::mbar_arrive_expect_tx(bar_v, 16384);
-    sm100::tma_load_3d(smem + I_V, &tm_v, bar_v, 0, it.h, (int)it.row0);
-    sm100::tma_load_3d(smem + I_V + 8192, &tm_v, bar_v, 64, it.h, (int)it.row0);
-  };
   // beta of an item, kept as raw bf16 bits in a register until its slot is free
   auto load_beta = [&](const Item& it) -> unsigned short {
     if (tid < C && tid < it.L)
@@ -258,14 +254,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     sm100::mbar_init(bar_q, 1);
     sm100::mbar_init(bar_g, 1);
     sm100::mbar_init(bar_k, 1);
-    sm100::mbar_init(bar_v, 1);
     sm100::mbar_init(bar_mma, 1);
     sm100::fence_mbar_init();
     if (cur.w < n_items) {
       load_g(cur);
       load_q(cur);
       load_k(cur);
-      load_v(cur);
     }
   }
   unsigned short beta_raw = cur.w < n_items ? load_beta(cur) : (unsigned short)0;
@@ -281,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint32_t mma_phase = 0;
   // items whose copies were issued / waited for, per barrier
   const int first = cur.w < n_items ? 1 : 0;
-  int q_issued = first, g_issued = first, k_issued = first, v_issued = first;
-  int q_done = 0, g_done = 0, k_done = 0, v_done = 0;
+  int q_issued = first, g_issued = first, k_issued = first;
+  int q_done = 0, g_done = 0, k_done = 0;
   auto wait_mma = [&]() {
     const bool ok = sm100::mbar_wait(bar_mma, mma_phase & 1);
     if (ok) ++mma_phase;
@@ -374,36 +368,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       wait_mma();
       if (tid == 32) sm100::bulk_wait_read();
     }
-    // (beta V)^T, K-major [value channel jv][row r], into the record; V is
-    // read before the gate passes overwrite it
-    if (!sm100::mbar_wait(bar_v, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
-    else v_done = li + 1;
-    {
-      // thread: value channels jv, jv + 1 (one bf16 pair per row) of rows
-      // 16 rq .. 16 rq + 15; beta of those rows in two 16-byte loads
-      const int jv = 2 * (tid & 63), rq = tid >> 6, cl = jv & 63;
-      const unsigned char* sv = smem + I_V + (jv >> 6) * 8192;
-      const uint4 bq0 = *reinterpret_cast<const uint4*>(smem + I_BETA + 32 * rq);
-      const uint4 bq1 = *reinterpret_cast<const uint4*>(smem + I_BETA + 32 * rq + 16);
-      const uint32_t bw[8] = {bq0.x, bq0.y, bq0.z, bq0.w, bq1.x, bq1.y, bq1.z, bq1.w};
-      float t0[16], t1[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int r = 16 * rq + e;
-        const uint32_t vv = *reinterpret_cast<const uint32_t*>(sv + row_off(r, cl));
-        const uint32_t bb = bw[e >> 1];
-        const float b = __uint_as_float((e & 1) ? (bb & 0xFFFF0000u) : (bb << 16));
-        const bool in = r < L;
-        t0[e] = in ? b * __uint_as_float(vv << 16) : 0.0f;
-        t1[e] = in ? b * __uint_as_float(vv & 0xFFFF0000u) : 0.0f;
-      }
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        st8_bf16(rec + REC_BV + k64_off(jv, 16 * rq + 8 * hh), t0 + 8 * hh);
-        st8_bf16(rec + REC_BV + k64_off(jv + 1, 16 * rq + 8 * hh), t1 + 8 * hh);
-      }
-    }
-    __syncthreads();
     SPLIT_MARK(2, mk);
 
     // ---- gate, pass hk: key channels 64 hk .. 64 hk + 63 -------------------
@@ -414,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     //   half 0: row e^{G_r - G_15}, col e^{G_15 - G_i}, cross col e^{G_31 - G_i}
     //   half 1: row e^{G_r - G_47}, col e^{G_47 - G_i}, cross row e^{G_r - G_31}
     // and the record's operands Q gamma (e^{G_r}), K dec (e^{G_C - G_r}),
-    // with (beta K gamma)^T kept for the W product.
+    // with (K gamma)^T kept for the W product (beta enters W through T).
     auto gate_pass = [&](const float (&al)[16], const int hk) {
       const int j = 64 * hk + jl;
       const unsigned char* sq = smem + I_Q + hk * 8192;
@@ -490,16 +454,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int i = 0; i < 8; ++i) t[i] = qE[i] * preq;
         st8_bf16(rec + REC_WQ + mn_off(64 + r0, j, 2048), t);
-        // (beta K gamma)^T, K-major [j][r] (beta of the 8 rows: one 16-byte load)
-        {
-          const uint4 bq = *reinterpret_cast<const uint4*>(smem + I_BETA + 2 * r0);
-          const uint32_t bw[4] = {bq.x, bq.y, bq.z, bq.w};
+        // (K gamma)^T, K-major [j][r]
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            t[i] = __uint_as_float((i & 1) ? (bw[i >> 1] & 0xFFFF0000u) : (bw[i >> 1] << 16)) *
-                   kE[i] * pre;
-        }
-        st8_bf16(smem + I_BKG + k64_off(j, r0), t);
+        for (int i = 0; i < 8; ++i) t[i] = kE[i] * pre;
+        st8_bf16(smem + I_KG + k64_off(j, r0), t);
         // (K e^{G_C - G})^T, K-major [j][r]
 #pragma unroll
         for (int i = 0; i < 8; ++i) t[i] = kF[i] * post;
@@ -649,36 +607,33 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (sync_aborted(s_abort)) break;
     SPLIT_MARK(7, mk);
 
-    // ---- T = (I + beta A_kk)^{-1} -------------------------------------------
+    // ---- T = (I + beta A_kk)^{-1}, written as T Diag(beta) ------------------
     unit_lower_inverse<AKK_LD>(s_akk, reinterpret_cast<float*>(smem + I_TF),
-                               reinterpret_cast<float*>(smem + I_Y), smem + I_T, tid);
+                               reinterpret_cast<float*>(smem + I_Y), smem + I_T, tid,
+                               [&](int i) { return beta_at(i); });
     sm100::fence_async_smem();
     sync_all();
     SPLIT_MARK(8, mk);
-    // T into the record by one bulk copy; the solve scratch (over V's and
-    // Q's landing zones) is dead: the next item's V and Q tiles
+    // T Diag(beta) into the record by one bulk copy; the solve scratch (over
+    // Q's landing zone) is dead: the next item's Q tiles
     if (tid == 32) {
       sm100::bulk_store(rec + REC_T, smem + I_T, 8192);
       sm100::bulk_commit();
     }
     if (has_next) {
-      if (tid == 32) {
-        load_v(nxt);
-        load_q(nxt);
-      }
-      v_issued = li + 2;
+      if (tid == 32) load_q(nxt);
       q_issued = li + 2;
     }
 
-    // ---- W^T = (beta K gamma)^T T^T (U = T (beta V) is formed by the state
-    //      kernel from the record's T and (beta V)^T) ------------------------
+    // ---- W^T = (K gamma)^T (T Diag(beta))^T (U = T Diag(beta) V is formed
+    //      by the state kernel from the record's T Diag(beta) and the input V)
     if (tid == 0) {
       const uint32_t idw = sm100::idesc_bf16(128, 64, 0, 0);
-      const uint32_t s_bkg = sm100::smem_u32(smem + I_BKG);
+      const uint32_t s_kg = sm100::smem_u32(smem + I_KG);
       const uint32_t s_t = sm100::smem_u32(smem + I_T);
 #pragma unroll
       for (int s = 0; s < C / 16; ++s)
-        sm100::mma_ss(tmem + TM_W, sm100::smem_desc(s_bkg + 256 * s, 128, 1024),
+        sm100::mma_ss(tmem + TM_W, sm100::smem_desc(s_kg + 256 * s, 128, 1024),
                       sm100::smem_desc(s_t + 256 * s, 128, 1024), idw, s > 0);
       sm100::mma_commit(bar_mma);
     }
@@ -706,7 +661,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (q_issued > q_done) sm100::mbar_wait(bar_q, q_done & 1, 200000000ull);
     if (g_issued > g_done) sm100::mbar_wait(bar_g, g_done & 1, 200000000ull);
     if (k_issued > k_done) sm100::mbar_wait(bar_k, k_done & 1, 200000000ull);
-    if (v_issued > v_done) sm100::mbar_wait(bar_v, v_done & 1, 200000000ull);
     if (mma_pending) sm100::mbar_wait(bar_mma, mma_phase & 1, 200000000ull);
   }
   if (tid == 32) sm100::bulk_wait();  // the last T copy
@@ -728,9 +682,10 @@ static_assert(S_SMEM <= 232448, "shared memory");
 constexpr uint32_t S_TM_COLS = 256;
 constexpr uint32_t TM_S = 0;    // state half: 128 lanes (key channel) x 64 columns
 constexpr uint32_t TM_P = 64;   // two buffers of [W S; Q gamma S (+ A_qk Delta)], 64 columns each
-constexpr uint32_t TM_U = 192;  // U = T (beta V) of the half (lanes 0..63 = rows)
+constexpr uint32_t TM_U = 192;  // U = T Diag(beta) V of the half (lanes 0..63 = rows)
 
-__global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitParams sp) {
+__global__ void __launch_bounds__(kThreads, 1)
+    kda_tc_state_kernel(const __grid_constant__ CUtensorMap tm_v8, const SplitParams sp) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const kda::FwdParams& p = sp.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -763,14 +718,20 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S_MISC);
   int* s_abort = reinterpret_cast<int*>(smem + S_MISC + 4);
 
-  auto issue = [&](int c) {  // record of chunk c into stage c & 1
+  // record of chunk c and this half's V tile into stage c & 1 (V: eight
+  // boxes of 8 value channels x 64 rows from the input, rows past the
+  // sequence's end are multiplied by zero columns of T Diag(beta))
+  auto issue = [&](int c) {
     unsigned char* st = smem + (c & 1) * STAGE_BYTES;
     const unsigned char* src = rec0 + (int64_t)c * REC_BYTES;
     uint64_t* bar = bar_full + (c & 1);
+    const int row = (int)(row_base + ((int64_t)sp.c_begin + c) * C);
     sm100::mbar_arrive_expect_tx(bar, STAGE_BYTES);
-    sm100::bulk_load(st + ST_KD, src + REC_KD, REC_BV - REC_KD, bar);
-    sm100::bulk_load(st + ST_BV, src + REC_BV + half * 8192, 8192, bar);
+    sm100::bulk_load(st + ST_KD, src + REC_KD, ST_COPY, bar);
     sm100::bulk_load(st + ST_GC, src + REC_GC, 512, bar);
+#pragma unroll
+    for (int g = 0; g < 8; ++g)
+      sm100::tma_load_3d(st + ST_V + 1024 * g, &tm_v8, bar, half * 64 + 8 * g, h, row);
   };
 
   if (warp == 0) {
@@ -865,16 +826,16 @@ __global__ void __launch_bounds__(kThreads, 1) kda_tc_state_kernel(const SplitPa
       record_error(p, s_abort, KDA_ERR_TIMEOUT);
     } else {
       landed = c + 1;
-      // U = [T; -] (beta V) of this half, while the CUDA cores copy S (the
-      // P product's commit covers it)
+      // U = [T Diag(beta); -] V of this half, while the CUDA cores copy S
+      // (the P product's commit covers it)
       if (tid == 0) {
-        const uint32_t idu = sm100::idesc_bf16(128, 64, 0, 0);
+        const uint32_t idu = sm100::idesc_bf16(128, 64, 0, 1);
         const uint32_t s_t = sm100::smem_u32(st + ST_T);
-        const uint32_t s_bv = sm100::smem_u32(st + ST_BV);
+        const uint32_t s_v = sm100::smem_u32(st + ST_V);
 #pragma unroll
         for (int k = 0; k < C / 16; ++k)
           sm100::mma_ss(tmem + TM_U, sm100::smem_desc(s_t + 256 * k, 128, 1024),
-                        sm100::smem_desc(s_bv + 256 * k, 128, 1024), idu, k > 0);
+                        sm100::smem_desc(s_v + 256 * k, 128, 1024), idu, k > 0);
         u_open = true;
       }
     }
@@ -1181,7 +1142,7 @@ namespace {
 // What every slice launch of one call shares: the tensor maps over the
 // inputs, the SM count, and where the records and the carried state live.
 struct SplitPlan {
-  CUtensorMap mq, mk, mg, mv;
+  CUtensorMap mq, mk, mg, mv8;  // mv8: V in boxes of 8 value channels (state kernel)
   int sms = 0;
   int nchunks = 0;
   size_t carry = 0, per = 0;   // bytes: carried state; records of one chunk column
@@ -1221,7 +1182,8 @@ kda_status plan_split(const kda::FwdParams& p, void* workspace, size_t workspace
   if (pl.sms < 1) return KDA_ERR_CUDA;
   // unswizzled tiles: every read of them goes along one row
   if (!make_map(&pl.mq, p.q, rows, p.H, DK, false) || !make_map(&pl.mk, p.k, rows, p.H, DK, false) ||
-      !make_map(&pl.mg, p.g, rows, p.H, DK, false) || !make_map(&pl.mv, p.v, rows, p.H, DV, false))
+      !make_map(&pl.mg, p.g, rows, p.H, DK, false) ||
+      !make_map(&pl.mv8, p.v, rows, p.H, DV, false, 8))
     return KDA_ERR_CUDA;
   if (kda_smem_attr((const void*)kda_tc_intra_kernel, I_SMEM) != KDA_OK ||
       kda_smem_attr((const void*)kda_tc_state_kernel, S_SMEM) != KDA_OK)
@@ -1257,11 +1219,11 @@ kda_status launch_slice(const kda::FwdParams& p, const SplitPlan& pl, int c0, in
     // persistent: two CTAs per SM walk the slice's (sequence, head, chunk) items
     const int64_t items = (int64_t)p.N * p.H * cnt;
     const int grid = items < 2 * (int64_t)pl.sms ? (int)items : 2 * pl.sms;
-    kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, pl.mv, sp);
+    kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, sp);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   }
   if (stages & 2) {
-    kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(sp);
+    kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(pl.mv8, sp);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   }
   return KDA_OK;
@@ -1291,9 +1253,9 @@ kda_status launch_packed(const kda::FwdParams& p, const SplitPlan& pl, cudaStrea
   sp.g_max = pl.g_max;
   const int64_t items = (int64_t)pl.g_max * p.H;
   const int grid = items < 2 * (int64_t)pl.sms ? (int)items : 2 * pl.sms;
-  kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, pl.mv, sp);
+  kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, sp);
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-  kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(sp);
+  kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(pl.mv8, sp);
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   return KDA_OK;
 }

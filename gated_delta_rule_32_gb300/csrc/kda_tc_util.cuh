@@ -109,16 +109,24 @@ __device__ __forceinline__ void store_tile(const float (&d)[4], float* D, int ld
   *reinterpret_cast<float2*>(r1) = make_float2(sc * d[2], sc * d[3]);
 }
 
-// bf16 copy of a 16x8 accumulator tile (scaled) into a K-major [r][i]
-// operand with K extent 64 (one packed pair per row and lane)
+// bf16 copy of a 16x8 accumulator tile into a K-major [r][i] operand with K
+// extent 64 (one packed pair per row and lane), column c scaled by cs(c)
+// times `sc`
+template <class ColScale>
 __device__ __forceinline__ void store_tile_bf16(const float (&d)[4], unsigned char* t, int row0,
-                                                int col0, float sc, int lane) {
+                                                int col0, float sc, int lane, ColScale cs) {
   const int g = lane >> 2, c0 = col0 + 2 * (lane & 3);
+  const float s0 = sc * cs(c0), s1 = sc * cs(c0 + 1);
   *reinterpret_cast<uint32_t*>(t + k64_off(row0 + g, c0)) =
-      sm100::pack_bf16x2(sc * d[0], sc * d[1]);
+      sm100::pack_bf16x2(s0 * d[0], s1 * d[1]);
   *reinterpret_cast<uint32_t*>(t + k64_off(row0 + g + 8, c0)) =
-      sm100::pack_bf16x2(sc * d[2], sc * d[3]);
+      sm100::pack_bf16x2(s0 * d[2], s1 * d[3]);
 }
+
+// column scales for unit_lower_inverse's bf16 output: none (T itself)
+struct NoColScale {
+  __device__ __forceinline__ float operator()(int) const { return 1.0f; }
+};
 
 // ---------------------------------------------------------------------------
 // T = (I + A)^{-1} for a strictly lower triangular 64 x 64 fp32 matrix A
@@ -136,12 +144,14 @@ __device__ __forceinline__ void store_tile_bf16(const float (&d)[4], unsigned ch
 // Called by all 256 threads of the CTA (it synchronises them, but not after
 // the last step).  A is read from `a` (row stride LD floats; blocks above
 // the block diagonal are never read), the strictly lower part of T is left
-// in `tf` (same stride), `y` ([32][36] fp32) is scratch, and T itself (unit
-// diagonal, zero above) is written as bf16 K-major [r][i] to `t_bf16`.
-// LD is a multiple of 4 (rows are read as float4).
-template <int LD>
+// in `tf` (same stride), `y` ([32][36] fp32) is scratch, and T Diag(cs) (T
+// with column i scaled by cs(i): unit diagonal times cs, zero above) is
+// written as bf16 K-major [r][i] to `t_bf16`; the fp32 copy in `tf` is T
+// itself.  LD is a multiple of 4 (rows are read as float4).
+template <int LD, class ColScale = NoColScale>
 __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, float* y,
-                                                   unsigned char* t_bf16, int tid) {
+                                                   unsigned char* t_bf16, int tid,
+                                                   ColScale cs = ColScale()) {
   static_assert(LD % 4 == 0, "row stride");
   const int warp = tid >> 5, lane = tid & 31;
   {
@@ -169,12 +179,13 @@ __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, fl
         if (4 * k4 + q > i) x[k4] = fmaf(-a_reg[k4][i], xi, x[k4]);
       }
     }
+    const float csc = cs(16 * blk + c);
 #pragma unroll
     for (int k4 = 0; k4 < 4; ++k4) {
       const int r = 16 * blk + 4 * k4 + q;
       tf[r * LD + 16 * blk + c] = x[k4];
       *reinterpret_cast<__nv_bfloat16*>(t_bf16 + k64_off(r, 16 * blk + c)) =
-          __float2bfloat16_rn(x[k4]);
+          __float2bfloat16_rn(x[k4] * csc);
     }
   }
   __syncthreads();
@@ -209,7 +220,7 @@ __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, fl
       mma_tf32(e2, af, ks ? bk1 : bk0);
     }
     store_tile(e2, tf, LD, 16 * a1, 16 * a0 + nt, -1.0f, lane);
-    store_tile_bf16(e2, t_bf16, 16 * a1, 16 * a0 + nt, -1.0f, lane);
+    store_tile_bf16(e2, t_bf16, 16 * a1, 16 * a0 + nt, -1.0f, lane, cs);
   } else {
     // zero the six 16 x 16 tiles above the block diagonal: 24 core matrices
     // of 128 bytes, written 16 bytes at a time
@@ -245,7 +256,7 @@ __device__ __forceinline__ void unit_lower_inverse(const float* a, float* tf, fl
     if (mt == 0) mma_tile<0, 16>(d, tf, LD, 32, 32, y, 36, 0, nt, lane);
     else mma_tile<0, 32>(d, tf, LD, 48, 32, y, 36, 0, nt, lane);
     store_tile(d, tf, LD, 32 + mt, nt, -1.0f, lane);
-    store_tile_bf16(d, t_bf16, 32 + mt, nt, -1.0f, lane);
+    store_tile_bf16(d, t_bf16, 32 + mt, nt, -1.0f, lane, cs);
   }
 }
 
@@ -275,15 +286,17 @@ inline PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// 3-D map over a [rows, H, d] bf16 tensor: box = 64 channels x 1 head x 64 rows,
-// rows 128B-swizzled in shared memory unless `swizzle` is false
+// 3-D map over a [rows, H, d] bf16 tensor: box = box_ch channels x 1 head x 64
+// rows, rows 128B-swizzled in shared memory unless `swizzle` is false (a box
+// of 8 channels, unswizzled, lands as 64 rows of 16 bytes: one column of
+// core matrices of an MN-major operand whose K index is the row)
 inline bool make_map(CUtensorMap* m, const void* base, int64_t rows, int H, int d,
-                     bool swizzle = true) {
+                     bool swizzle = true, int box_ch = 64) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
-  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t box[3] = {(cuuint32_t)box_ch, 1, 64};
   cuuint32_t es[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,

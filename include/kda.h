@@ -125,7 +125,7 @@ kda_status kda_chunk_fwd_f32(const float* q, const float* k, const float* v,
  *               256-byte aligned.  The two-kernel path (KDA_ALGO_SPLIT)
  *               also accepts less for a dense batch, down to one chunk
  *               record per (sequence, head) plus the carried state
- *               (N * H * (82432 + 65536) bytes, rounded up to 256): it then
+ *               (N * H * (66048 + 65536) bytes, rounded up to 256): it then
  *               runs the sequence in more, shorter slices; below that
  *               KDA_ERR_WORKSPACE.  A packed batch needs the full size
  *               (every chunk column, ceil(T / 64) + N at most, at once).

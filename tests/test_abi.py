@@ -98,7 +98,7 @@ def test_staging_bytes_of_the_pipelined_host_call(lib):
     qk = B * T * H * 128 * 2
     state = B * H * 128 * 128 * 4
     fixed = 3 * r256(qk) + 2 * r256(qk) + r256(B * T * H * 2) + 2 * r256(state) + 256
-    piece = r256(state) + B * H * 82432 * 64
+    piece = r256(state) + B * H * 66048 * 64
     n = kda.kda_host_staging_bytes(B, T, H, 128, 128, kda.KDA_BF16, 1, 1, 0)
     assert n == fixed + r256(piece)
     # a single chunk is not cut: the whole-call workspace
@@ -120,17 +120,17 @@ def test_package_fails_loudly_without_library(tmp_path):
 
 def test_split_path_host_checks(lib):
     # workspace sizing of the two-kernel path: carried state + one slice of
-    # 82432-byte chunk records per (sequence, head); a packed batch keeps
+    # 66048-byte chunk records per (sequence, head); a packed batch keeps
     # every chunk column (ceil(T / 64) + N of them at most) at once, after
     # its chunk offsets and chunk table
     carry = 2 * 32 * 128 * 128 * 4
     nb = kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=kda.KDA_ALGO_SPLIT)
-    assert nb == carry + 2 * 32 * 512 * 82432
+    assert nb == carry + 2 * 32 * 512 * 66048
     assert kda.kda_workspace_bytes(2, 100, 1, 128, 128, algo=kda.KDA_ALGO_SPLIT) == \
-        2 * 128 * 128 * 4 + 2 * 2 * 82432
+        2 * 128 * 128 * 4 + 2 * 2 * 66048
     g_max = 32768 // 64 + 2
     assert kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=kda.KDA_ALGO_SPLIT,
-                                   packed=1) == carry + 256 + 4352 + 32 * g_max * 82432
+                                   packed=1) == carry + 256 + 4352 + 32 * g_max * 66048
     assert g_max * 8 <= 4352
     assert kda.kda_resolve_algo(kda.KDA_BF16, 128, 128, 0, kda.KDA_ALGO_SPLIT) == \
         kda.KDA_ALGO_SPLIT

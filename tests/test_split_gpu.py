@@ -19,7 +19,7 @@ from kda_inputs import WORKLOADS, make_inputs, make_unit, small_workload
 pytestmark = pytest.mark.gpu
 
 SPLIT = kda.KDA_ALGO_SPLIT
-REC = 82432  # bytes of one chunk record
+REC = 66048  # bytes of one chunk record
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -161,8 +161,10 @@ def test_split_deterministic_and_close_to_fused():
     of, sf = pkg.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
                          algo=kda.KDA_ALGO_TC)
     torch.cuda.synchronize()
-    assert rel(a[0], of.float().cpu().numpy()) <= 1e-2
-    assert rel(a[1], sf.cpu().numpy()) <= 1e-2
+    # two approximations of the same forward, each within 1e-2 of the oracle
+    # (the paths round U at different points): within 2e-2 of each other
+    assert rel(a[0], of.float().cpu().numpy()) <= 2e-2
+    assert rel(a[1], sf.cpu().numpy()) <= 2e-2
 
 
 def test_full_b2_h32_t32k_split_sampled():
@@ -238,8 +240,11 @@ def run_packed(x, algo=SPLIT, status=None, workspace=True):
                                          ((65, 0, 0, 128), 0.02)])
 def test_split_packed_matches_oracle(lens, s0_std):
     """Sequences of every kind of length (empty, one token, partial and
-    whole chunks) packed in one batch: parity with the oracle, and the same
-    result as the fused kernel within the rounding of the shared operands."""
+    whole chunks) packed in one batch: parity with the oracle, and agreement
+    with the fused kernel.  The two paths round U at different points (T
+    Diag(beta) times V here, T times bf16(beta V) there), so they are
+    compared by the triangle bound: each within 1e-2 of the oracle, so within
+    2e-2 of each other."""
     w = small_workload("pk", B=1, T=sum(lens), H=3, dk=128, dv=128, seed=41, varlen=True,
                        lengths=lens, s0_std=s0_std)
     x = make_inputs(w)
@@ -252,7 +257,7 @@ def test_split_packed_matches_oracle(lens, s0_std):
     np.testing.assert_array_equal(o, o2)
     np.testing.assert_array_equal(s, s2)
     of, sf = run_packed(x, algo=kda.KDA_ALGO_TC, workspace=False)
-    assert rel(o, of) <= 1e-2 and rel(s, sf) <= 1e-2
+    assert rel(o, of) <= 2e-2 and rel(s, sf) <= 2e-2
 
 
 def test_split_packed_bad_seqlens_reported():
