@@ -20,7 +20,7 @@ struct ProbeArgs {
   int32_t* status;
   int M, N, K;
   int a_mode;  // 0 smem K-major, 1 smem MN-major, 2 tmem
-  int b_mode;  // 0 smem K-major, 1 smem MN-major
+  int b_mode;  // 0 smem K-major, 1 smem MN-major, 2 smem MN-major 128-byte swizzle (N = 64)
   int pack;    // 0: core matrices adjacent along K first; 1: along M/N first
 };
 
@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(kProbeThreads) umma_probe_kernel(ProbeArgs a) 
   const int tid = threadIdx.x, warp = tid / 32;
   unsigned char* sA = smem;                 // 32 KiB
   unsigned char* sB = smem + 32768;         // 64 KiB (+ slack after)
+  // a swizzled operand starts on a 1024-byte boundary (its atoms' alignment)
+  sB += (1024u - (sm100::smem_u32(sB) & 1023u)) & 1023u;
   const int M = a.M, N = a.N, K = a.K;
 
   if (warp == 0) {
@@ -63,10 +65,22 @@ __global__ void __launch_bounds__(kProbeThreads) umma_probe_kernel(ProbeArgs a) 
   op_off(0, 0, M, K, a.a_mode == 1, a.pack, lbo_a, sbo_a);
   for (int e = tid; e < N * K; e += kProbeThreads) {
     int r = e / K, k = e % K;
-    uint32_t o = op_off(r, k, N, K, a.b_mode == 1, a.pack, lbo_b, sbo_b);
+    uint32_t o;
+    if (a.b_mode == 2) {
+      // element (n, k): atom k / 8, row k % 8 of it (128 bytes), 16-byte chunk
+      // n / 8 stored at chunk (n / 8) ^ (k % 8)
+      o = (uint32_t)(k >> 3) * 1024u + (uint32_t)(k & 7) * 128u +
+          ((uint32_t)(((r >> 3) ^ (k & 7)) & 7) << 4) + (uint32_t)(r & 7) * 2u;
+    } else {
+      o = op_off(r, k, N, K, a.b_mode == 1, a.pack, lbo_b, sbo_b);
+    }
     *reinterpret_cast<uint16_t*>(sB + o) = a.B[e];
   }
-  op_off(0, 0, N, K, a.b_mode == 1, a.pack, lbo_b, sbo_b);
+  if (a.b_mode == 2) {
+    lbo_b = 1024; sbo_b = 1024;  // one atom along N: only the K-atom stride matters
+  } else {
+    op_off(0, 0, N, K, a.b_mode == 1, a.pack, lbo_b, sbo_b);
+  }
   sm100::tc_fence_before();
   __syncthreads();
   sm100::tc_fence_after();
@@ -100,9 +114,11 @@ __global__ void __launch_bounds__(kProbeThreads) umma_probe_kernel(ProbeArgs a) 
   __syncthreads();
   sm100::tc_fence_after();
   if (tid == 0) {
-    const uint32_t idesc = sm100::idesc_bf16(M, N, a.a_mode == 1, a.b_mode == 1);
+    const uint32_t idesc = sm100::idesc_bf16(M, N, a.a_mode == 1, a.b_mode != 0);
     for (int s = 0; s < K / 16; ++s) {
-      uint64_t bd = sm100::smem_desc(sm100::smem_u32(sB) + s * 2 * lbo_b, lbo_b, sbo_b);
+      uint64_t bd = a.b_mode == 2
+                        ? sm100::smem_desc_sw128(sm100::smem_u32(sB) + s * 2048, lbo_b, sbo_b)
+                        : sm100::smem_desc(sm100::smem_u32(sB) + s * 2 * lbo_b, lbo_b, sbo_b);
       if (a.a_mode == 2) {
         sm100::mma_ts(tbase + d_col, tbase + a_col + 8 * s, bd, idesc, s > 0);
       } else {
@@ -140,9 +156,10 @@ extern "C" kda_status kda_debug_umma(const uint16_t* A, const uint16_t* B, float
   if (M != 64 && M != 128) return KDA_ERR_UNSUPPORTED;
   if (K < 16 || K > 128 || K % 16) return KDA_ERR_UNSUPPORTED;
   if (N < 16 || N > 256 || N % 16) return KDA_ERR_UNSUPPORTED;
-  if (a_mode < 0 || a_mode > 2 || b_mode < 0 || b_mode > 1 || pack < 0 || pack > 1)
+  if (a_mode < 0 || a_mode > 2 || b_mode < 0 || b_mode > 2 || pack < 0 || pack > 1)
     return KDA_ERR_INVALID_ARG;
   if (a_mode == 2 && M != 128) return KDA_ERR_UNSUPPORTED;
+  if (b_mode == 2 && N != 64) return KDA_ERR_UNSUPPORTED;
   ProbeArgs p{A, B, D, dev_status, M, N, K, a_mode, b_mode, pack};
   const int smem = 32768 + 65536 + 65536;  // operands + slack
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

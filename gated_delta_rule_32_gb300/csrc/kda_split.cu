@@ -50,14 +50,17 @@ constexpr int REC_GC = 65536;    // gamma_C fp32 [128]                          
 constexpr int REC_BYTES = 66048;
 // what one state CTA holds per chunk: the record (KD | AQ | WQ | T Diag(beta)
 // by one bulk copy, gamma_C by another) and the 64 value channels of its half
-// of V, loaded from the input by TMA in 8-channel boxes, each box 64 rows x
-// 16 bytes: together an MN-major operand (N = value channel, K = row; K
-// groups 128 B apart, N groups 1024 B apart).  U = T Diag(beta) V of the half
+// of V, loaded from the input by one TMA box of 64 rows x 128 bytes with the
+// 128-byte swizzle: an MN-major operand (N = value channel, K = row) in
+// swizzle atoms of 8 rows, 1024 bytes apart.  U = T Diag(beta) V of the half
 // is formed there, on the tensor cores, into tensor memory: its rows past 63
-// read the V tile that follows T and are never used.
+// read the V tile that follows T and are never used.  Stages are a multiple
+// of 1024 bytes, so the V tile stays aligned to its atoms.
 constexpr int ST_KD = 0, ST_AQ = 16384, ST_WQ = 24576, ST_T = 57344, ST_V = 65536,
               ST_GC = 73728;
-constexpr int STAGE_BYTES = 74240;
+constexpr int STAGE_BYTES = 74752;
+static_assert(STAGE_BYTES % 1024 == 0 && ST_V % 1024 == 0, "swizzle atoms of V");
+static_assert(ST_GC + 512 <= STAGE_BYTES, "stage");
 constexpr int ST_COPY = REC_GC;  // bytes of the record's first bulk copy
 static_assert(ST_V == ST_T + 8192, "U operand rows");
 static_assert(ST_COPY == ST_V, "first bulk copy ends where V starts");
@@ -685,7 +688,7 @@ constexpr uint32_t TM_P = 64;   // two buffers of [W S; Q gamma S (+ A_qk Delta)
 constexpr uint32_t TM_U = 192;  // U = T Diag(beta) V of the half (lanes 0..63 = rows)
 
 __global__ void __launch_bounds__(kThreads, 1)
-    kda_tc_state_kernel(const __grid_constant__ CUtensorMap tm_v8, const SplitParams sp) {
+    kda_tc_state_kernel(const __grid_constant__ CUtensorMap tm_v, const SplitParams sp) {
   extern __shared__ __align__(1024) unsigned char smem[];
   const kda::FwdParams& p = sp.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -718,20 +721,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S_MISC);
   int* s_abort = reinterpret_cast<int*>(smem + S_MISC + 4);
 
-  // record of chunk c and this half's V tile into stage c & 1 (V: eight
-  // boxes of 8 value channels x 64 rows from the input, rows past the
-  // sequence's end are multiplied by zero columns of T Diag(beta))
+  // record of chunk c and this half's V tile into stage c & 1 (V: one box of
+  // 64 value channels x 64 rows from the input; rows past the sequence's end
+  // are multiplied by zero columns of T Diag(beta))
   auto issue = [&](int c) {
     unsigned char* st = smem + (c & 1) * STAGE_BYTES;
     const unsigned char* src = rec0 + (int64_t)c * REC_BYTES;
     uint64_t* bar = bar_full + (c & 1);
     const int row = (int)(row_base + ((int64_t)sp.c_begin + c) * C);
-    sm100::mbar_arrive_expect_tx(bar, STAGE_BYTES);
+    sm100::mbar_arrive_expect_tx(bar, ST_COPY + 512 + 8192);
     sm100::bulk_load(st + ST_KD, src + REC_KD, ST_COPY, bar);
     sm100::bulk_load(st + ST_GC, src + REC_GC, 512, bar);
-#pragma unroll
-    for (int g = 0; g < 8; ++g)
-      sm100::tma_load_3d(st + ST_V + 1024 * g, &tm_v8, bar, half * 64 + 8 * g, h, row);
+    sm100::tma_load_3d(st + ST_V, &tm_v, bar, half * 64, h, row);
   };
 
   if (warp == 0) {
@@ -835,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < C / 16; ++k)
           sm100::mma_ss(tmem + TM_U, sm100::smem_desc(s_t + 256 * k, 128, 1024),
-                        sm100::smem_desc(s_v + 256 * k, 128, 1024), idu, k > 0);
+                        sm100::smem_desc_sw128(s_v + 2048 * k, 1024, 1024), idu, k > 0);
         u_open = true;
       }
     }
@@ -1142,7 +1143,7 @@ namespace {
 // What every slice launch of one call shares: the tensor maps over the
 // inputs, the SM count, and where the records and the carried state live.
 struct SplitPlan {
-  CUtensorMap mq, mk, mg, mv8;  // mv8: V in boxes of 8 value channels (state kernel)
+  CUtensorMap mq, mk, mg, mv;  // mv: V, 128-byte swizzled (state kernel)
   int sms = 0;
   int nchunks = 0;
   size_t carry = 0, per = 0;   // bytes: carried state; records of one chunk column
@@ -1183,7 +1184,7 @@ kda_status plan_split(const kda::FwdParams& p, void* workspace, size_t workspace
   // unswizzled tiles: every read of them goes along one row
   if (!make_map(&pl.mq, p.q, rows, p.H, DK, false) || !make_map(&pl.mk, p.k, rows, p.H, DK, false) ||
       !make_map(&pl.mg, p.g, rows, p.H, DK, false) ||
-      !make_map(&pl.mv8, p.v, rows, p.H, DV, false, 8))
+      !make_map(&pl.mv, p.v, rows, p.H, DV, true))
     return KDA_ERR_CUDA;
   if (kda_smem_attr((const void*)kda_tc_intra_kernel, I_SMEM) != KDA_OK ||
       kda_smem_attr((const void*)kda_tc_state_kernel, S_SMEM) != KDA_OK)
@@ -1223,7 +1224,7 @@ kda_status launch_slice(const kda::FwdParams& p, const SplitPlan& pl, int c0, in
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   }
   if (stages & 2) {
-    kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(pl.mv8, sp);
+    kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(pl.mv, sp);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   }
   return KDA_OK;
@@ -1255,7 +1256,7 @@ kda_status launch_packed(const kda::FwdParams& p, const SplitPlan& pl, cudaStrea
   const int grid = items < 2 * (int64_t)pl.sms ? (int)items : 2 * pl.sms;
   kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, sp);
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-  kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(pl.mv8, sp);
+  kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(pl.mv, sp);
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   return KDA_OK;
 }

@@ -195,6 +195,14 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
+// The same descriptor for an operand laid out with the 128-byte swizzle (the
+// layout a TMA load with CU_TENSOR_MAP_SWIZZLE_128B writes): atoms of 8 rows
+// x 128 bytes, 1024-byte aligned, whose 16-byte chunks are permuted by the
+// row index within the atom.  Swizzle-mode field (bits 61-63) = 2.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(saddr, lbo, sbo) | ((uint64_t)2 << 61);
+}
+
 // Instruction descriptor, kind::f16 with BF16 A/B and FP32 accumulation.
 // a_mn / b_mn: 1 if that operand is MN-major in shared memory.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {

@@ -279,7 +279,8 @@ kda_status kda_debug_intra(const uint16_t* q, const uint16_t* k, const uint16_t*
  * [128][N] fp32 receives all 128 accumulator lanes (lanes an M = 64 tile
  * does not write hold a NaN marker).  M in {64, 128}; N in 16..256 and K in
  * 16..128, multiples of 16.  a_mode: 0 shared K-major, 1 shared MN-major,
- * 2 tensor memory (M = 128 only); b_mode: 0 K-major, 1 MN-major; pack:
+ * 2 tensor memory (M = 128 only); b_mode: 0 K-major, 1 MN-major, 2 MN-major
+ * with the 128-byte swizzle (N = 64: one swizzle atom wide); pack:
  * order of the 8x16-byte core matrices (0: along K first, 1: along M/N
  * first).  One CTA; asynchronous on `stream`.
  */

@@ -57,3 +57,13 @@ def test_m64_lane_placement():
     print("M=64 lane of each row:", {r: found.get(r) for r in range(64)})
     assert sorted(found) == list(range(64))
     assert all(len(v) == 1 for v in found.values())
+
+
+@pytest.mark.parametrize("K", [16, 64, 128])
+@pytest.mark.parametrize("a_mode", [0, 1])
+def test_tile_product_swizzled_mn_major_b(K, a_mode):
+    # B in the layout a 128-byte-swizzled TMA load of a [K rows][64 channels]
+    # tile writes (the state kernel's V operand)
+    D, ref = run(128, 64, K, a_mode, 2, 0, seed=K + 7)
+    err = (D - ref).abs().max().item() / ref.abs().max().item()
+    assert err < 1e-5, err
