@@ -29,6 +29,8 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "kda_common.cuh"
 #include "sm100.cuh"
 #include "kda_tc_util.cuh"
@@ -78,7 +80,14 @@ struct SplitParams {
   const int2* chunk_tab;  // [g_max], null for dense batches
   const int* chunk_off;   // [N + 1]
   int g_max;              // chunk columns: ceil(T / 64) + N bounds the true count
+  // test hook (0 in every normal call): bit 0 makes the intra kernel's first
+  // wait, bit 1 the state kernel's first wait, wait on a barrier that nothing
+  // ever completes, with a 1 ms limit, so that the timeout and abort path runs
+  int stall_test;
 };
+
+// limit of the waits the stall test makes run out
+constexpr unsigned long long kStallTestNs = 1000000ull;
 
 #ifdef KDA_PHASE_TIMING
 // cycles per phase, summed over the CTAs of (sequence 0, head 0) for the
@@ -219,6 +228,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint64_t* bar_g = bar_q + 1;                                   // decay-logit tiles
   uint64_t* bar_k = bar_q + 2;                                   // K tiles
   uint64_t* bar_mma = bar_q + 3;
+  uint64_t* bar_never = bar_q + 4;  // stall test only: nothing arrives on it
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + I_MISC);
   int* s_abort = reinterpret_cast<int*>(smem + I_MISC + 4);
   unsigned short* s_beta_raw = reinterpret_cast<unsigned short*>(smem + I_BETA);
@@ -258,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     sm100::mbar_init(bar_g, 1);
     sm100::mbar_init(bar_k, 1);
     sm100::mbar_init(bar_mma, 1);
+    sm100::mbar_init(bar_never, 1);
     sm100::fence_mbar_init();
     if (cur.w < n_items) {
       load_g(cur);
@@ -318,7 +329,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     const Item nxt = next_of(cur);
     const bool has_next = nxt.w < n_items;
     const uint32_t par = (uint32_t)(li & 1);
-    if (!sm100::mbar_wait(bar_g, par)) record_error(p, s_abort, KDA_ERR_TIMEOUT);
+    const bool stall = (sp.stall_test & 1) && li == 0;
+    if (!(stall ? sm100::mbar_wait(bar_never, 0, kStallTestNs) : sm100::mbar_wait(bar_g, par)))
+      record_error(p, s_abort, KDA_ERR_TIMEOUT);
     else g_done = li + 1;
     if (tid < C) s_beta_raw[tid] = beta_raw;  // bf16 bits; readers widen them
     // rows past the end of the sequence (its last chunk only): a decay logit
@@ -718,6 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem + S_BAR);  // [2]
   uint64_t* bar_mma = bar_full + 2;
+  uint64_t* bar_never = bar_full + 3;  // stall test only: nothing arrives on it
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + S_MISC);
   int* s_abort = reinterpret_cast<int*>(smem + S_MISC + 4);
 
@@ -743,6 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm100::mbar_init(bar_full, 1);
     sm100::mbar_init(bar_full + 1, 1);
     sm100::mbar_init(bar_mma, 1);
+    sm100::mbar_init(bar_never, 1);
     sm100::fence_mbar_init();
     if (nc > 0) issue(0);
     if (nc > 1) issue(1);
@@ -823,7 +838,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int s = c & 1;
     const unsigned char* st = smem + s * STAGE_BYTES;
     const uint32_t tm_p = TM_P + 64 * s;
-    if (!sm100::mbar_wait(bar_full + s, (uint32_t)((c >> 1) & 1))) {
+    const bool stall = (sp.stall_test & 2) && c == 0;
+    if (!(stall ? sm100::mbar_wait(bar_never, 0, kStallTestNs)
+                : sm100::mbar_wait(bar_full + s, (uint32_t)((c >> 1) & 1)))) {
       record_error(p, s_abort, KDA_ERR_TIMEOUT);
     } else {
       landed = c + 1;
@@ -1077,6 +1094,9 @@ __global__ void kda_split_table_kernel(const int32_t* cu, const int* off, int N,
   }
 }
 
+// the stall test's flags for the next calls (test hook, see SplitParams)
+std::atomic<int> g_stall_test{0};
+
 // default bytes of records held at once (the slice length follows from it)
 constexpr size_t kRecordBudget = (size_t)4 << 30;
 
@@ -1216,6 +1236,7 @@ kda_status launch_slice(const kda::FwdParams& p, const SplitPlan& pl, int c0, in
   sp.g_max = 0;
   sp.s_in = c0 == 0 ? p.init_state : pl.through;
   sp.s_out = c0 + cnt == pl.nchunks ? p.final_state : pl.through;
+  sp.stall_test = g_stall_test.load();
   if (stages & 1) {
     // persistent: two CTAs per SM walk the slice's (sequence, head, chunk) items
     const int64_t items = (int64_t)p.N * p.H * cnt;
@@ -1252,6 +1273,7 @@ kda_status launch_packed(const kda::FwdParams& p, const SplitPlan& pl, cudaStrea
   sp.chunk_tab = pl.chunk_tab;
   sp.chunk_off = pl.chunk_off;
   sp.g_max = pl.g_max;
+  sp.stall_test = g_stall_test.load();
   const int64_t items = (int64_t)pl.g_max * p.H;
   const int grid = items < 2 * (int64_t)pl.sms ? (int)items : 2 * pl.sms;
   kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, sp);
@@ -1321,4 +1343,13 @@ extern "C" kda_status kda_split_stage(int stage, const uint16_t* q, const uint16
   p.N = B; p.T = T; p.H = H; p.dk = DK; p.dv = DV; p.scale = scale;
   return run_split(p, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), stage,
                    true);
+}
+
+// Test hook: the next calls of the two-kernel path make their first wait in
+// the intra kernel (flags bit 0) and / or the state kernel (bit 1) run out
+// (see SplitParams::stall_test); 0 restores normal calls.
+extern "C" kda_status kda_debug_stall_test(int flags) {
+  if (flags < 0 || flags > 3) return KDA_ERR_INVALID_ARG;
+  g_stall_test.store(flags);
+  return KDA_OK;
 }

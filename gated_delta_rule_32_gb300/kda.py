@@ -60,6 +60,7 @@ _SIGS = {
     "kda_split_stage": (_i, [_i] + [_vp] * 8 + [_i] * 3 + [ctypes.c_float, _vp, ctypes.c_size_t,
                                                         _vp, _vp]),
     "kda_debug_intra": (_i, [_vp] * 5 + [_i] * 5 + [_vp, _i, _i] + [_vp] * 6 + [_vp]),
+    "kda_debug_stall_test": (_i, [_i]),
 }
 
 
@@ -255,3 +256,9 @@ def forward(q, k, v, g_logit, beta, init_state=None, cu_seqlens=None, scale=1.0,
     if rc != KDA_OK:
         raise KdaError("kda_chunk_fwd_ex", rc)
     return out, fs
+
+
+def kda_debug_stall_test(flags: int) -> int:
+    """Test hook: make the two-kernel path's first waits run out (bit 0 intra
+    kernel, bit 1 state kernel); 0 restores normal calls."""
+    return load().kda_debug_stall_test(int(flags))

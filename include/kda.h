@@ -304,6 +304,20 @@ kda_status kda_split_stage(int stage, const uint16_t* q, const uint16_t* k, cons
                            int T, int H, float scale, void* workspace, size_t workspace_bytes,
                            int32_t* dev_status, kda_stream_t stream);
 
+/*
+ * Test hook for the bounded waits of the two-kernel path: after
+ * kda_debug_stall_test(flags), calls on that path make their first wait in
+ * the intra-chunk kernel (flags bit 0) and / or in the state kernel (bit 1)
+ * wait, with a 1 ms limit, on a barrier that nothing ever completes.  The
+ * wait gives up, the kernel records KDA_ERR_TIMEOUT in dev_status, waits
+ * (bounded) for the copies it has in flight, frees its tensor memory and
+ * returns; the outputs of such a call are unspecified.  flags = 0 restores
+ * normal calls.  Process-wide; not thread-safe against concurrent calls.
+ * Returns KDA_ERR_INVALID_ARG for flags outside 0..3.  No counterpart on
+ * the pages: it exists to test the library's own failure path.
+ */
+kda_status kda_debug_stall_test(int flags);
+
 /* The path family kda_chunk_fwd_ex would take for these arguments:
  * KDA_ALGO_SIMT, KDA_ALGO_TC (AUTO on the tensor cores: fused, segmented or
  * two-kernel form by the sizes) or KDA_ALGO_SPLIT when asked for; -1 if the

@@ -179,3 +179,9 @@ def test_allocation_free_entry_has_the_same_argument_rules(lib):
     assert st(nseg=1) == kda.KDA_ERR_INVALID_ARG
     # past the fixed scratch array: refused before any device work
     assert st(H=32, nseg=8) == kda.KDA_ERR_WORKSPACE
+
+
+def test_stall_test_hook_flags(lib):
+    assert kda.kda_debug_stall_test(4) == kda.KDA_ERR_INVALID_ARG
+    assert kda.kda_debug_stall_test(-1) == kda.KDA_ERR_INVALID_ARG
+    assert kda.kda_debug_stall_test(0) == kda.KDA_OK
