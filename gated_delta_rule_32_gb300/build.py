@@ -16,6 +16,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkda.so")
+# the debug build (-DKDA_DEBUG: device-side bounds checks that report
+# KDA_ERR_BOUNDS instead of trapping), kept apart from the normal library
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libkda.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -39,15 +43,15 @@ def _deps():
         [os.path.join(INCLUDE, "kda.h")]
 
 
-def _up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def _up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+def _compile(src: str, extra, build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src).replace(".cu", ".o"))
     cmd = [nvcc()] + ARCH + NVCC_FLAGS + list(extra) + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -57,26 +61,30 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    """Compile every csrc/*.cu for sm_103a and link _build/libkda.so."""
-    os.makedirs(BUILD, exist_ok=True)
-    if not force and not extra and _up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra=(), debug: bool = False) -> str:
+    """Compile every csrc/*.cu for sm_103a and link _build/libkda.so (with
+    debug=True: the bounds-checking build, _build_debug/libkda.so)."""
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    if debug:
+        extra = list(extra) + ["-DKDA_DEBUG"]
+    os.makedirs(build_dir, exist_ok=True)
+    if not force and (debug or not extra) and _up_to_date(lib):
+        return lib
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + ".tmp%d" % os.getpid()
+        objs = list(ex.map(lambda s: _compile(s, extra, build_dir), srcs))
+    tmp = lib + ".tmp%d" % os.getpid()
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
-        print("built", LIB)
-    return LIB
+        print("built", lib)
+    return lib
 
 
 if __name__ == "__main__":
     force = "--force" in sys.argv
     extra = ["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else []
-    build(force=force or bool(extra), verbose=True, extra=extra)
+    build(force=force or bool(extra), verbose=True, extra=extra, debug="--debug" in sys.argv)

@@ -227,12 +227,19 @@ const char* kda_status_string(kda_status s) {
     case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: bounded on-chip wait gave up";
     case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
     case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace too small";
+    case KDA_ERR_BOUNDS: return "KDA_ERR_BOUNDS: device-side bounds check failed (debug build)";
   }
   return "KDA_ERR_UNKNOWN";
 }
 
 const char* kda_build_info(void) {
-  return "libkda: KDA chunked forward, sm_103a (tcgen05/TMEM/TMA fused path + fp32 CUDA-core path)";
+#ifdef KDA_DEBUG
+  return "libkda: KDA chunked forward, sm_103a (tcgen05/TMEM/TMA tensor-core paths + fp32 "
+         "CUDA-core path), debug build with device-side bounds checks";
+#else
+  return "libkda: KDA chunked forward, sm_103a (tcgen05/TMEM/TMA tensor-core paths + fp32 "
+         "CUDA-core path)";
+#endif
 }
 
 int kda_resolve_algo(int dtype, int dk, int dv, int chunk_size, int algo) {

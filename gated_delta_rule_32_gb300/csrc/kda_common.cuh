@@ -9,6 +9,14 @@
 
 namespace kda {
 
+// Device-side bounds checks of the debug build (-DKDA_DEBUG): a failed check
+// records KDA_ERR_BOUNDS and skips the access instead of trapping.
+#ifdef KDA_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
 // Floor on the per-step log-decay: each step keeps at least e^-5 ~ 0.67% of
 // its state (Kimi K3 architecture, orkas.ai, "A lower bound that erased a
 // GPU code path").

@@ -80,6 +80,10 @@ struct SplitParams {
   const int2* chunk_tab;  // [g_max], null for dense batches
   const int* chunk_off;   // [N + 1]
   int g_max;              // chunk columns: ceil(T / 64) + N bounds the true count
+  // extents the debug build checks accesses against: chunk records the
+  // workspace holds, token rows of the input tensors
+  int64_t rec_items;
+  int64_t rows;
   // test hook (0 in every normal call): bit 0 makes the intra kernel's first
   // wait, bit 1 the state kernel's first wait, wait on a barrier that nothing
   // ever completes, with a 1 ms limit, so that the timeout and abort path runs
@@ -258,8 +262,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
   // beta of an item, kept as raw bf16 bits in a register until its slot is free
   auto load_beta = [&](const Item& it) -> unsigned short {
-    if (tid < C && tid < it.L)
+    if (tid < C && tid < it.L) {
+      if (kda::kDebugChecks && (it.row0 + tid < 0 || it.row0 + tid >= sp.rows)) return 0;
       return static_cast<const unsigned short*>(p.beta)[(it.row0 + tid) * H + it.h];
+    }
     return 0;
   };
   Item cur = item_of(blockIdx.x);
@@ -326,6 +332,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int li = 0; cur.w < n_items; ++li) {
     const int L = cur.L;
     unsigned char* rec = sp.rec + cur.ri * (int64_t)REC_BYTES;
+    // debug build: the item's record and rows inside their buffers, else the
+    // loop ends at the first barrier below, before any global store
+    if (kda::kDebugChecks &&
+        (cur.ri < 0 || cur.ri >= sp.rec_items || cur.row0 < 0 || cur.row0 + L > sp.rows))
+      record_error(p, s_abort, KDA_ERR_BOUNDS);
     const Item nxt = next_of(cur);
     const bool has_next = nxt.w < n_items;
     const uint32_t par = (uint32_t)(li & 1);
@@ -728,6 +739,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     rec0 = sp.rec + ((int64_t)n * H + h) * (int64_t)sp.c_count * REC_BYTES;
   }
   const int64_t sbase = ((int64_t)n * H + h) * (int64_t)DK * DV + half * 64;
+  // debug build: this chain's records and rows inside their buffers, else it
+  // does nothing but report (every thread takes the same decision)
+  bool dbg_bad = false;
+  if (kda::kDebugChecks) {
+    const int64_t first = nc > 0 ? (int64_t)(rec0 - sp.rec) / REC_BYTES : 0;
+    dbg_bad = first < 0 || first + nc > sp.rec_items || row_base < 0 ||
+              row_base + seq_len > sp.rows;
+    if (dbg_bad) nc = 0;
+  }
 
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(smem + S_BAR);  // [2]
   uint64_t* bar_mma = bar_full + 2;
@@ -768,6 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm100::tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_q = 32u * (warp & 3);
+  if (dbg_bad && tid == 0 && p.dev_status) atomicExch(p.dev_status, (int32_t)KDA_ERR_BOUNDS);
 
   // entry state into TMEM (lane = key channel)
   if (warp < 4) {
@@ -986,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     SPLIT_MARK(22, mk);
   }
 
-  if (*s_abort) {
+  if (*s_abort || dbg_bad) {
     // bounded waits for copies and products still in flight (a U product
     // that no commit follows gets one first)
     if (tid == 0 && u_open) {
@@ -1096,6 +1117,12 @@ __global__ void kda_split_table_kernel(const int32_t* cu, const int* off, int N,
 
 // the stall test's flags for the next calls (test hook, see SplitParams)
 std::atomic<int> g_stall_test{0};
+// debug builds: records the kernels are told the workspace holds (0: real)
+std::atomic<long long> g_record_capacity{0};
+int64_t told_capacity(int64_t real) {
+  const long long o = g_record_capacity.load();
+  return o > 0 && o < real ? o : real;
+}
 
 // default bytes of records held at once (the slice length follows from it)
 constexpr size_t kRecordBudget = (size_t)4 << 30;
@@ -1237,6 +1264,8 @@ kda_status launch_slice(const kda::FwdParams& p, const SplitPlan& pl, int c0, in
   sp.s_in = c0 == 0 ? p.init_state : pl.through;
   sp.s_out = c0 + cnt == pl.nchunks ? p.final_state : pl.through;
   sp.stall_test = g_stall_test.load();
+  sp.rec_items = told_capacity((int64_t)p.N * p.H * cnt);
+  sp.rows = (int64_t)p.N * p.T;
   if (stages & 1) {
     // persistent: two CTAs per SM walk the slice's (sequence, head, chunk) items
     const int64_t items = (int64_t)p.N * p.H * cnt;
@@ -1274,6 +1303,8 @@ kda_status launch_packed(const kda::FwdParams& p, const SplitPlan& pl, cudaStrea
   sp.chunk_off = pl.chunk_off;
   sp.g_max = pl.g_max;
   sp.stall_test = g_stall_test.load();
+  sp.rec_items = told_capacity((int64_t)pl.g_max * p.H);
+  sp.rows = p.T;
   const int64_t items = (int64_t)pl.g_max * p.H;
   const int grid = items < 2 * (int64_t)pl.sms ? (int)items : 2 * pl.sms;
   kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, sp);
@@ -1351,5 +1382,13 @@ extern "C" kda_status kda_split_stage(int stage, const uint16_t* q, const uint16
 extern "C" kda_status kda_debug_stall_test(int flags) {
   if (flags < 0 || flags > 3) return KDA_ERR_INVALID_ARG;
   g_stall_test.store(flags);
+  return KDA_OK;
+}
+
+// Test hook of the debug build (see kda.h): the record capacity the kernels
+// are told; 0 restores the real one.
+extern "C" kda_status kda_debug_record_capacity(int64_t items) {
+  if (items < 0) return KDA_ERR_INVALID_ARG;
+  g_record_capacity.store((long long)items);
   return KDA_OK;
 }

@@ -24,6 +24,7 @@ KDA_ERR_BAD_SEQLENS = 4
 KDA_ERR_TIMEOUT = 5
 KDA_ERR_CUDA = 6
 KDA_ERR_WORKSPACE = 7
+KDA_ERR_BOUNDS = 8
 KDA_BF16 = 0
 KDA_F32 = 1
 KDA_ALGO_AUTO = 0
@@ -61,6 +62,7 @@ _SIGS = {
                                                         _vp, _vp]),
     "kda_debug_intra": (_i, [_vp] * 5 + [_i] * 5 + [_vp, _i, _i] + [_vp] * 6 + [_vp]),
     "kda_debug_stall_test": (_i, [_i]),
+    "kda_debug_record_capacity": (_i, [ctypes.c_int64]),
 }
 
 
@@ -262,3 +264,8 @@ def kda_debug_stall_test(flags: int) -> int:
     """Test hook: make the two-kernel path's first waits run out (bit 0 intra
     kernel, bit 1 state kernel); 0 restores normal calls."""
     return load().kda_debug_stall_test(int(flags))
+
+
+def kda_debug_record_capacity(items: int) -> int:
+    """Debug builds: the chunk-record capacity the kernels are told (0 = real)."""
+    return load().kda_debug_record_capacity(int(items))

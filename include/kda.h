@@ -72,7 +72,8 @@ typedef enum {
   KDA_ERR_BAD_SEQLENS = 4,  /* cu_seqlens not 0 .. T non-decreasing (device-detected) */
   KDA_ERR_TIMEOUT = 5,      /* a bounded on-chip wait gave up (device-detected) */
   KDA_ERR_CUDA = 6,         /* a CUDA runtime call failed */
-  KDA_ERR_WORKSPACE = 7     /* workspace given but smaller than kda_workspace_bytes() */
+  KDA_ERR_WORKSPACE = 7,    /* workspace given but smaller than kda_workspace_bytes() */
+  KDA_ERR_BOUNDS = 8        /* a device-side bounds check failed (KDA_DEBUG builds only) */
 } kda_status;
 
 typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
@@ -317,6 +318,19 @@ kda_status kda_split_stage(int stage, const uint16_t* q, const uint16_t* k, cons
  * the pages: it exists to test the library's own failure path.
  */
 kda_status kda_debug_stall_test(int flags);
+
+/*
+ * Debug builds (compiled with -DKDA_DEBUG; kda_build_info() says so): the
+ * two-kernel path checks, on the device, every chunk record index against
+ * the records the workspace holds and every token row against the input,
+ * before it touches global memory; a failed check records KDA_ERR_BOUNDS in
+ * dev_status, skips the access and ends the kernel as a timeout does.  This
+ * hook makes the next calls' kernels believe the workspace holds only
+ * `items` chunk records (0 = the real count), so that the checks can be
+ * seen to fire while every access stays inside the real buffer.  No effect
+ * in normal builds.  Process-wide; not thread-safe against concurrent calls.
+ */
+kda_status kda_debug_record_capacity(int64_t items);
 
 /* The path family kda_chunk_fwd_ex would take for these arguments:
  * KDA_ALGO_SIMT, KDA_ALGO_TC (AUTO on the tensor cores: fused, segmented or

@@ -24,7 +24,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         s = kda.status_string(code)
         assert s.startswith("KDA_")
     assert kda.status_string(99) == "KDA_ERR_UNKNOWN"
