@@ -30,6 +30,8 @@
 #include <string.h>
 
 #include <atomic>
+#include <map>
+#include <mutex>
 
 #include "kda_common.cuh"
 #include "sm100.cuh"
@@ -1249,13 +1251,15 @@ kda_status plan_split(const kda::FwdParams& p, void* workspace, size_t workspace
 }
 
 // One slice, chunks [c0, c0 + cnt) of every sequence: the intra kernel over
-// it, then the state kernel.  `stages` selects the kernels (bit 0 intra,
-// bit 1 state).
+// it (on `s_intra`, at most `grid_cap` CTAs), then the state kernel (on
+// `s_state`), the records at `rec`.  `stages` selects the kernels (bit 0
+// intra, bit 1 state).
 kda_status launch_slice(const kda::FwdParams& p, const SplitPlan& pl, int c0, int cnt,
-                        cudaStream_t stream, int stages) {
+                        cudaStream_t s_intra, cudaStream_t s_state, int stages,
+                        unsigned char* rec, int grid_cap) {
   SplitParams sp;
   sp.p = p;
-  sp.rec = pl.rec;
+  sp.rec = rec;
   sp.c_begin = c0;
   sp.c_count = cnt;
   sp.chunk_tab = nullptr;
@@ -1269,15 +1273,93 @@ kda_status launch_slice(const kda::FwdParams& p, const SplitPlan& pl, int c0, in
   if (stages & 1) {
     // persistent: two CTAs per SM walk the slice's (sequence, head, chunk) items
     const int64_t items = (int64_t)p.N * p.H * cnt;
-    const int grid = items < 2 * (int64_t)pl.sms ? (int)items : 2 * pl.sms;
-    kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, sp);
+    const int grid = items < (int64_t)grid_cap ? (int)items : grid_cap;
+    kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, s_intra>>>(pl.mq, pl.mk, pl.mg, sp);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   }
   if (stages & 2) {
-    kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(pl.mv, sp);
+    kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, s_state>>>(pl.mv, sp);
     if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   }
   return KDA_OK;
+}
+
+// Streams and events of the overlapped slice schedule, created once per
+// device (the state stream at the highest priority, so that its CTAs are
+// placed first) and used under one lock for a call's whole enqueue sequence.
+struct OverlapRes {
+  cudaStream_t s_intra = nullptr, s_state = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_intra[2] = {}, ev_state[2] = {};
+};
+std::mutex g_ov_mu;
+std::map<int, OverlapRes> g_ov;
+
+// (called with g_ov_mu held)
+kda_status overlap_res(OverlapRes** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+  auto it = g_ov.find(dev);
+  if (it != g_ov.end()) {
+    *out = &it->second;
+    return KDA_OK;
+  }
+  OverlapRes r;
+  int least = 0, greatest = 0;
+  bool ok = cudaDeviceGetStreamPriorityRange(&least, &greatest) == cudaSuccess &&
+            cudaStreamCreateWithPriority(&r.s_intra, cudaStreamNonBlocking, least) ==
+                cudaSuccess &&
+            cudaStreamCreateWithPriority(&r.s_state, cudaStreamNonBlocking, greatest) ==
+                cudaSuccess &&
+            cudaEventCreateWithFlags(&r.ev_start, cudaEventDisableTiming) == cudaSuccess;
+  for (int b = 0; b < 2 && ok; ++b)
+    ok = cudaEventCreateWithFlags(&r.ev_intra[b], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&r.ev_state[b], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) return KDA_ERR_CUDA;
+  *out = &(g_ov[dev] = r);
+  return KDA_OK;
+}
+
+// Slices of a dense batch whose state chains leave most SMs idle (few
+// sequence x head pairs, long sequences): slice i + 1's intra kernel runs on
+// the SMs the state CTAs leave free while slice i's state pass runs, the
+// records alternating between the two halves of the record buffer.  The
+// kernels never wait on one another: the library's two streams order them
+// by events (slice i's state after its intra kernel; slice i + 2's intra
+// kernel after slice i's state pass has read that half).  The result is the
+// same as one slice after another.
+kda_status run_overlapped(const kda::FwdParams& p, const SplitPlan& pl, int slice,
+                          cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_ov_mu);
+  OverlapRes* r = nullptr;
+  kda_status st = overlap_res(&r);
+  if (st != KDA_OK) return st;
+  const int state_ctas = 2 * p.N * p.H;
+  const int cap_alone = 2 * pl.sms, cap_beside = 2 * (pl.sms - state_ctas);
+  unsigned char* half[2] = {pl.rec, pl.rec + pl.per * (size_t)slice};
+  auto cu = [&](cudaError_t e) {
+    if (e != cudaSuccess && st == KDA_OK) st = KDA_ERR_CUDA;
+  };
+  cu(cudaEventRecord(r->ev_start, stream));
+  cu(cudaStreamWaitEvent(r->s_intra, r->ev_start, 0));
+  cu(cudaStreamWaitEvent(r->s_state, r->ev_start, 0));
+  int last = 0;
+  for (int i = 0, c0 = 0; c0 < pl.nchunks && st == KDA_OK; ++i, c0 += slice) {
+    const int b = i & 1, cnt = pl.nchunks - c0 < slice ? pl.nchunks - c0 : slice;
+    if (i >= 2) cu(cudaStreamWaitEvent(r->s_intra, r->ev_state[b], 0));
+    if (st == KDA_OK)
+      st = launch_slice(p, pl, c0, cnt, r->s_intra, r->s_state, 1, half[b],
+                        i == 0 ? cap_alone : cap_beside);
+    cu(cudaEventRecord(r->ev_intra[b], r->s_intra));
+    cu(cudaStreamWaitEvent(r->s_state, r->ev_intra[b], 0));
+    if (st == KDA_OK)
+      st = launch_slice(p, pl, c0, cnt, r->s_intra, r->s_state, 2, half[b], cap_alone);
+    cu(cudaEventRecord(r->ev_state[b], r->s_state));
+    last = b;
+  }
+  // the caller's stream continues once the last state pass is done (which
+  // follows every intra kernel)
+  cu(cudaStreamWaitEvent(stream, r->ev_state[last], 0));
+  return st;
 }
 
 // The slices run back to back on `stream`; `one_slice` refuses a workspace
@@ -1322,9 +1404,16 @@ kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_
   if (pl.packed) return stages == 3 ? launch_packed(p, pl, stream) : KDA_ERR_UNSUPPORTED;
   const int slice = pl.fit < (size_t)pl.nchunks ? (int)pl.fit : pl.nchunks;
   if (one_slice && slice < pl.nchunks) return KDA_ERR_WORKSPACE;
+  // more than one slice and state chains on at most half of the SMs: the
+  // overlapped schedule (not while the caller's stream is being captured)
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (stages == 3 && !one_slice && slice < pl.nchunks && pl.fit >= 2 &&
+      4 * (int64_t)p.N * p.H <= pl.sms &&
+      cudaStreamIsCapturing(stream, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone)
+    return run_overlapped(p, pl, (int)(pl.fit / 2), stream);
   for (int c0 = 0; c0 < pl.nchunks && st == KDA_OK; c0 += slice)
     st = launch_slice(p, pl, c0, pl.nchunks - c0 < slice ? pl.nchunks - c0 : slice, stream,
-                      stages);
+                      stream, stages, pl.rec, 2 * pl.sms);
   return st;
 }
 
@@ -1346,7 +1435,7 @@ kda_status kda_run_split_range(const kda::FwdParams& p, void* workspace, size_t 
   kda_status st = plan_split(p, workspace, workspace_bytes, pl);
   if (st != KDA_OK) return st;
   if (c0 < 0 || cnt < 1 || c0 + cnt > pl.nchunks || (size_t)cnt > pl.fit) return KDA_ERR_INVALID_ARG;
-  return launch_slice(p, pl, c0, cnt, stream, 3);
+  return launch_slice(p, pl, c0, cnt, stream, stream, 3, pl.rec, 2 * pl.sms);
 }
 
 // Device bytes of the two-kernel path for slices of `chunks` chunks.

@@ -108,7 +108,11 @@ def test_split_degenerate_gates(case):
 
 @pytest.mark.parametrize("extra_chunks", [0, 1, 3])
 def test_slices_bit_identical(extra_chunks):
-    # 11 chunks with a ragged tail; slices of 1, 2 and 4 chunks
+    # 11 chunks with a ragged tail; slices of 1 chunk (room for 1 per chain:
+    # one slice after another) and, with room for 2 or 4 chunks, slices of 1
+    # and 2 chunks on the overlapped schedule (4 chains leave most SMs idle:
+    # the next slice's intra kernel runs beside the current state pass, the
+    # records alternating between the two halves of the buffer)
     w = small_workload("sl", B=2, T=690, H=2, dk=128, dv=128, s0_std=0.05, seed=21)
     x = make_inputs(w)
     o1, s1 = run(x)
