@@ -44,6 +44,7 @@ int kda_device_sms() {
 }
 
 size_t kda_split_packed_workspace_bytes(int N, int T, int H);
+size_t kda_split_packed_min_workspace_bytes(int N, int T, int H);
 
 namespace {
 
@@ -126,19 +127,15 @@ bool use_tc(int dtype, int dk, int dv, int chunk_size, int algo) {
 
 // The two-kernel form of the tensor-core path, when asked for or by default
 // (it runs every chunk's state-independent work at once; the fused kernel
-// repeats it per value half and runs it serially per chain).  A packed batch
-// keeps all its chunk records at once, so by default it takes this form only
-// while they fit in 4 GiB, else the fused kernel; KDA_ALGO_TC always takes
-// the fused kernel.
+// repeats it per value half and runs it serially per chain), dense or packed
+// (long batches in slices of chunks or of chunk columns); KDA_ALGO_TC always
+// takes the fused kernel.
 bool use_split(int dtype, int dk, int dv, int chunk_size, int algo, int packed, int N, int T,
                int H) {
+  (void)H;
   if (T < 1 || !use_tc(dtype, dk, dv, chunk_size, algo)) return false;
   if (algo != KDA_ALGO_SPLIT && algo != KDA_ALGO_AUTO) return false;
-  if (packed) {
-    if (N < 1 || N >= (1 << 24)) return false;
-    if (algo == KDA_ALGO_AUTO && kda_split_packed_workspace_bytes(N, T, H) > ((size_t)4 << 30))
-      return false;
-  }
+  if (packed && (N < 1 || N >= (1 << 24))) return false;
   return true;
 }
 
@@ -184,9 +181,9 @@ bool host_pipelined(int dtype, int dk, int dv, int packed, int T) {
 // sequence in more, shorter slices.
 static kda_status run_split_ws(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream) {
-  const bool packed = p.cu_seqlens != nullptr;  // (all records at once: no slices)
+  const bool packed = p.cu_seqlens != nullptr;
   if (workspace) {
-    const size_t min_bytes = packed ? kda_split_packed_workspace_bytes(p.N, p.T, p.H)
+    const size_t min_bytes = packed ? kda_split_packed_min_workspace_bytes(p.N, p.T, p.H)
                                     : kda_split_min_workspace_bytes(p.N, p.H);
     if (workspace_bytes < min_bytes) return KDA_ERR_WORKSPACE;
     return kda_run_split(p, workspace, workspace_bytes, stream);

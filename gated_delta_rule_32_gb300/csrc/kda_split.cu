@@ -71,17 +71,19 @@ static_assert(ST_COPY == ST_V, "first bulk copy ends where V starts");
 
 struct SplitParams {
   kda::FwdParams p;
-  unsigned char* rec;  // records: dense [N][H][c_count], packed [H][g_max]
+  unsigned char* rec;  // records: dense [N][H][c_count], packed [H][g_count]
   int c_begin;         // first chunk of the slice (dense)
   int c_count;         // chunks in the slice (dense)
   const float* s_in;   // state entering the slice [N][H][DK][DV] (null: zero)
   float* s_out;        // state leaving the slice (null: not kept)
-  // packed batches (cu_seqlens; one slice): sequence n owns the chunk
-  // columns [chunk_off[n], chunk_off[n + 1]); column g starts at token row
-  // chunk_tab[g].x and holds chunk_tab[g].y >> 24 rows (0: no chunk)
+  // packed batches (cu_seqlens): sequence n owns the chunk columns
+  // [chunk_off[n], chunk_off[n + 1]); column g starts at token row
+  // chunk_tab[g].x and holds chunk_tab[g].y >> 24 rows (0: no chunk); a
+  // slice is the columns [g_begin, g_begin + g_count)
   const int2* chunk_tab;  // [g_max], null for dense batches
   const int* chunk_off;   // [N + 1]
   int g_max;              // chunk columns: ceil(T / 64) + N bounds the true count
+  int g_begin, g_count;
   // extents the debug build checks accesses against: chunk records the
   // workspace holds, token rows of the input tensors
   int64_t rec_items;
@@ -156,12 +158,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5;
   const int H = p.H;
   // work items: dense w = (n * H + h) * c_count + chunk of the slice,
-  // packed w = chunk column * H + h; this CTA takes blockIdx.x,
+  // packed w = chunk column of the slice * H + h; this CTA takes blockIdx.x,
   // blockIdx.x + gridDim.x, ...
   const bool packed = sp.chunk_tab != nullptr;
-  const int64_t n_items = packed ? (int64_t)sp.g_max * H : (int64_t)p.N * H * sp.c_count;
+  const int64_t n_items = packed ? (int64_t)sp.g_count * H : (int64_t)p.N * H * sp.c_count;
   struct Item {
-    int n, h, cl;    // sequence, head, chunk of the slice (packed: chunk column)
+    int n, h, cl;    // sequence, head, chunk of the slice (packed: column of the slice)
     int L;           // valid rows of the chunk
     int64_t row0;    // global row of its first token
     int64_t w;
@@ -169,11 +171,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
   auto finish = [&](Item& it) {
     if (packed) {  // (read well before its first use, the next item's tiles)
-      const int2 e = it.w < n_items ? sp.chunk_tab[it.cl] : make_int2(0, 0);
+      const int2 e = it.w < n_items ? sp.chunk_tab[sp.g_begin + it.cl] : make_int2(0, 0);
       it.row0 = e.x;
       it.n = e.y & 0xFFFFFF;
       it.L = (e.y >> 24) & 0x7F;
-      it.ri = (int64_t)it.h * sp.g_max + it.cl;
+      it.ri = (int64_t)it.h * sp.g_count + it.cl;
     } else {
       const int64_t cs = ((int64_t)sp.c_begin + it.cl) * C;
       it.L = (p.T - cs) < C ? (int)(p.T - cs) : C;
@@ -723,19 +725,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   long long t_mark = clock64();
   const bool mk = tid == 0 && half == 0 && h == 0 && n == 0;
 #endif
-  // this sequence: its chunks (of the slice), records, first token row and
-  // length
-  int nc;
+  // this sequence: its chunks of the slice (the first one is chunk c_first
+  // of the sequence), their records, its first token row and length, and
+  // where its state enters and leaves the slice
+  int nc, c_first;
   int64_t row_base, seq_len;
   const unsigned char* rec0;
+  const float* s_in = sp.s_in;
+  float* s_out = sp.s_out;
+  bool involved = true;  // false: the sequence has nothing in this slice
   if (sp.chunk_tab) {
-    const int c_lo = sp.chunk_off[n];
-    nc = sp.chunk_off[n + 1] - c_lo;
+    const int c_lo = sp.chunk_off[n], c_hi = sp.chunk_off[n + 1];
+    const int g0 = sp.g_begin, g1 = sp.g_begin + sp.g_count;
+    const int lo = c_lo > g0 ? c_lo : g0, hi = c_hi < g1 ? c_hi : g1;
+    nc = hi > lo ? hi - lo : 0;
+    c_first = lo - c_lo;
     row_base = p.cu_seqlens[n];
     seq_len = p.cu_seqlens[n + 1] - row_base;
-    rec0 = sp.rec + ((int64_t)h * sp.g_max + c_lo) * REC_BYTES;
+    rec0 = sp.rec + ((int64_t)h * sp.g_count + (lo - g0)) * REC_BYTES;
+    // an empty sequence belongs to the slice its (empty) column range starts in
+    involved = nc > 0 || (c_lo == c_hi && c_lo >= g0 && c_lo < g1);
+    s_in = c_lo >= g0 ? p.init_state : sp.s_in;      // starts here, or carried in
+    s_out = c_hi <= g1 ? p.final_state : sp.s_out;   // ends here, or carried on
   } else {
     nc = sp.c_count;
+    c_first = sp.c_begin;
     row_base = (int64_t)n * p.T;
     seq_len = p.T;
     rec0 = sp.rec + ((int64_t)n * H + h) * (int64_t)sp.c_count * REC_BYTES;
@@ -764,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* st = smem + (c & 1) * STAGE_BYTES;
     const unsigned char* src = rec0 + (int64_t)c * REC_BYTES;
     uint64_t* bar = bar_full + (c & 1);
-    const int row = (int)(row_base + ((int64_t)sp.c_begin + c) * C);
+    const int row = (int)(row_base + ((int64_t)c_first + c) * C);
     sm100::mbar_arrive_expect_tx(bar, ST_COPY + 512 + 8192);
     sm100::bulk_load(st + ST_KD, src + REC_KD, ST_COPY, bar);
     sm100::bulk_load(st + ST_GC, src + REC_GC, 512, bar);
@@ -799,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t r[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e)
-        r[e] = __float_as_uint(sp.s_in ? sp.s_in[sbase + (int64_t)i * DV + c + e] : 0.0f);
+        r[e] = __float_as_uint(s_in && involved ? s_in[sbase + (int64_t)i * DV + c + e] : 0.0f);
       sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + c), r);
     }
     sm100::tmem_wait_st();
@@ -830,7 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // output rows of chunk c (warps 6-7: TMEM lanes 64..127 = rows 0..63)
   auto write_out = [&](int c) {
     const int r = tid - 192;
-    const int64_t cs = ((int64_t)sp.c_begin + c) * C;
+    const int64_t cs = ((int64_t)c_first + c) * C;
     const int L = (seq_len - cs) < C ? (int)(seq_len - cs) : C;
     float o[64];
 #pragma unroll
@@ -987,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     //     this warp rescales next, so program order alone keeps the read
     //     ahead of the next chunk's rescaling)
     if (p.ckpt) {
-      const int64_t cs = ((int64_t)sp.c_begin + c) * C;
+      const int64_t cs = ((int64_t)c_first + c) * C;
       const int L = (seq_len - cs) < C ? (int)(seq_len - cs) : C;
       const int64_t done = cs + L;
       if (L == C && done % p.ckpt_every == 0 && done / p.ckpt_every <= p.ckpt_max) {
@@ -1021,9 +1035,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       sm100::mbar_wait(bar_full + (k & 1), (uint32_t)((k >> 1) & 1), 200000000ull);
   } else {
     if (nc > 0 && warp >= 6) write_out(nc - 1);
-    if (sp.s_out && warp < 4) {
+    if (s_out && involved && warp < 4) {
       const int i = tid;
-      float* dst = sp.s_out + sbase + (int64_t)i * DV;
+      float* dst = s_out + sbase + (int64_t)i * DV;
       for (int c16 = 0; c16 < 64; c16 += 16) {
         float v[16];
         sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c16), v);
@@ -1132,29 +1146,42 @@ constexpr size_t kRecordBudget = (size_t)4 << 30;
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t carry_bytes(int N, int H) { return align256((size_t)N * H * DK * DV * sizeof(float)); }
 
-// packed batches, one slice: [carry][chunk_off: N + 1 ints][chunk_tab:
-// g_max entries][records: H x g_max]
+// packed batches: [carry][chunk_off: N + 1 ints][chunk_tab: g_max
+// entries][records: H x the chunk columns of one slice]
 int packed_g_max(int N, int T) { return (int)(((int64_t)T + C - 1) / C + N); }
 struct PackedLayout {
   size_t off_at, tab_at, rec_at, total;
 };
-PackedLayout packed_layout(int N, int T, int H) {
+PackedLayout packed_layout(int N, int T, int H, int64_t cols) {
   PackedLayout L;
   const size_t g = (size_t)packed_g_max(N, T);
   L.off_at = carry_bytes(N, H);
   L.tab_at = L.off_at + align256((size_t)(N + 1) * sizeof(int));
   L.rec_at = L.tab_at + align256(g * sizeof(int2));
-  L.total = L.rec_at + g * (size_t)H * REC_BYTES;
+  L.total = L.rec_at + (size_t)cols * H * REC_BYTES;
   return L;
+}
+// chunk columns per slice of the default workspace: all of them while their
+// records fit in the record budget
+int64_t packed_default_cols(int N, int T, int H) {
+  const int64_t g = packed_g_max(N, T);
+  int64_t fit = (int64_t)(kRecordBudget / ((size_t)H * REC_BYTES));
+  if (fit < 1) fit = 1;
+  return g < fit ? g : fit;
 }
 
 }  // namespace
 
 // Device bytes of the two-kernel path for a packed batch of T tokens in N
-// sequences (all chunk records at once).
+// sequences: by default the chunk records of every column while they fit in
+// the record budget (else slices of columns); at least one column's records.
 size_t kda_split_packed_workspace_bytes(int N, int T, int H) {
   if (N < 1 || H < 1 || T < 1) return 0;
-  return packed_layout(N, T, H).total;
+  return packed_layout(N, T, H, packed_default_cols(N, T, H)).total;
+}
+size_t kda_split_packed_min_workspace_bytes(int N, int T, int H) {
+  if (N < 1 || H < 1 || T < 1) return 0;
+  return packed_layout(N, T, H, 1).total;
 }
 
 #ifdef KDA_PHASE_TIMING
@@ -1216,12 +1243,14 @@ kda_status plan_split(const kda::FwdParams& p, void* workspace, size_t workspace
   if (((uintptr_t)workspace & 255) != 0) return KDA_ERR_MISALIGNED;
   pl.carry = carry_bytes(p.N, p.H);
   if (pl.packed) {
-    const PackedLayout L = packed_layout(p.N, p.T, p.H);
+    const PackedLayout L = packed_layout(p.N, p.T, p.H, 1);
     if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     pl.g_max = packed_g_max(p.N, p.T);
     pl.chunk_off = reinterpret_cast<int*>(ws + L.off_at);
     pl.chunk_tab = reinterpret_cast<int2*>(ws + L.tab_at);
+    pl.per = (size_t)p.H * REC_BYTES;  // records of one chunk column
+    pl.fit = (workspace_bytes - L.rec_at) / pl.per;
   } else {
     pl.per = (size_t)p.N * p.H * REC_BYTES;
     if (workspace_bytes < pl.carry + pl.per) return KDA_ERR_WORKSPACE;
@@ -1238,14 +1267,13 @@ kda_status plan_split(const kda::FwdParams& p, void* workspace, size_t workspace
   if (kda_smem_attr((const void*)kda_tc_intra_kernel, I_SMEM) != KDA_OK ||
       kda_smem_attr((const void*)kda_tc_state_kernel, S_SMEM) != KDA_OK)
     return KDA_ERR_CUDA;
-  if (pl.packed) {
-    pl.rec = static_cast<unsigned char*>(workspace) + packed_layout(p.N, p.T, p.H).rec_at;
-    pl.through = nullptr;
-    return KDA_OK;
-  }
   // the state crosses slices in final_state when there is one (each CTA
   // reads its part before it writes it), else in the workspace
   pl.through = p.final_state ? p.final_state : static_cast<float*>(workspace);
+  if (pl.packed) {
+    pl.rec = static_cast<unsigned char*>(workspace) + packed_layout(p.N, p.T, p.H, 1).rec_at;
+    return KDA_OK;
+  }
   pl.rec = static_cast<unsigned char*>(workspace) + pl.carry;
   return KDA_OK;
 }
@@ -1265,6 +1293,8 @@ kda_status launch_slice(const kda::FwdParams& p, const SplitPlan& pl, int c0, in
   sp.chunk_tab = nullptr;
   sp.chunk_off = nullptr;
   sp.g_max = 0;
+  sp.g_begin = 0;
+  sp.g_count = 0;
   sp.s_in = c0 == 0 ? p.init_state : pl.through;
   sp.s_out = c0 + cnt == pl.nchunks ? p.final_state : pl.through;
   sp.stall_test = g_stall_test.load();
@@ -1364,8 +1394,8 @@ kda_status run_overlapped(const kda::FwdParams& p, const SplitPlan& pl, int slic
 
 // The slices run back to back on `stream`; `one_slice` refuses a workspace
 // that would need more than one slice.
-// A packed batch in one slice: its chunk table, then both kernels over every
-// chunk column.
+// A packed batch: its chunk table, then both kernels over each slice of
+// chunk columns in turn (one slice when the workspace holds every column).
 kda_status launch_packed(const kda::FwdParams& p, const SplitPlan& pl, cudaStream_t stream) {
   kda_split_offsets_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.N, p.T, pl.chunk_off,
                                                    p.dev_status);
@@ -1374,25 +1404,33 @@ kda_status launch_packed(const kda::FwdParams& p, const SplitPlan& pl, cudaStrea
   kda_split_table_kernel<<<tb, 256, 0, stream>>>(p.cu_seqlens, pl.chunk_off, p.N, pl.g_max,
                                                  pl.chunk_tab);
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-  SplitParams sp;
-  sp.p = p;
-  sp.rec = pl.rec;
-  sp.c_begin = 0;
-  sp.c_count = 0;
-  sp.s_in = p.init_state;
-  sp.s_out = p.final_state;
-  sp.chunk_tab = pl.chunk_tab;
-  sp.chunk_off = pl.chunk_off;
-  sp.g_max = pl.g_max;
-  sp.stall_test = g_stall_test.load();
-  sp.rec_items = told_capacity((int64_t)pl.g_max * p.H);
-  sp.rows = p.T;
-  const int64_t items = (int64_t)pl.g_max * p.H;
-  const int grid = items < 2 * (int64_t)pl.sms ? (int)items : 2 * pl.sms;
-  kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, sp);
-  if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-  kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(pl.mv, sp);
-  if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+  const int fit = pl.fit < (size_t)pl.g_max ? (int)pl.fit : pl.g_max;
+  for (int g0 = 0; g0 < pl.g_max; g0 += fit) {
+    const int cnt = pl.g_max - g0 < fit ? pl.g_max - g0 : fit;
+    SplitParams sp;
+    sp.p = p;
+    sp.rec = pl.rec;
+    sp.c_begin = 0;
+    sp.c_count = 0;
+    // sequences start from init_state and end in final_state; one that
+    // spans slices carries its state through final_state or the workspace
+    sp.s_in = pl.through;
+    sp.s_out = pl.through;
+    sp.chunk_tab = pl.chunk_tab;
+    sp.chunk_off = pl.chunk_off;
+    sp.g_max = pl.g_max;
+    sp.g_begin = g0;
+    sp.g_count = cnt;
+    sp.stall_test = g_stall_test.load();
+    sp.rec_items = told_capacity((int64_t)cnt * p.H);
+    sp.rows = p.T;
+    const int64_t items = (int64_t)cnt * p.H;
+    const int grid = items < 2 * (int64_t)pl.sms ? (int)items : 2 * pl.sms;
+    kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, sp);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+    kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(pl.mv, sp);
+    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
+  }
   return KDA_OK;
 }
 

@@ -144,6 +144,18 @@ def test_split_path_host_checks(lib):
     assert kda.kda_split_stage(2, **dict(st, T=0)) == kda.KDA_ERR_INVALID_ARG
 
 
+def test_packed_workspace_sizes(lib):
+    # [carry][chunk offsets][chunk table][records of a slice of chunk columns]
+    def r256(x):
+        return (x + 255) // 256 * 256
+    N, T, H = 3, 1 << 20, 16
+    g_max = T // 64 + N
+    rec_at = r256(N * H * 128 * 128 * 4) + r256((N + 1) * 4) + r256(g_max * 8)
+    cols = (4 << 30) // (H * 66048)
+    assert cols < g_max
+    assert kda.kda_workspace_bytes(N, T, H, 128, 128, packed=1) == rec_at + cols * H * 66048
+
+
 def test_resolve_path(lib):
     # the automatic path of a bf16 batch is the two-kernel form (a packed one
     # while all its chunk records fit in 4 GiB, else the fused kernel), fp32
@@ -151,7 +163,9 @@ def test_resolve_path(lib):
     rp = kda.kda_resolve_path
     assert rp(2, 32768, 32) == kda.KDA_ALGO_SPLIT
     assert rp(2, 32768, 32, packed=True) == kda.KDA_ALGO_SPLIT
-    assert rp(1, 1 << 20, 16, packed=True) == kda.KDA_ALGO_TC
+    # a packed batch too long to hold every chunk record at once runs in
+    # slices of chunk columns, its default workspace capped at 4 GiB of records
+    assert rp(1, 1 << 20, 16, packed=True) == kda.KDA_ALGO_SPLIT
     assert rp(2, 32768, 32, algo=kda.KDA_ALGO_TC) == kda.KDA_ALGO_TC
     assert rp(2, 100, 4, dtype=kda.KDA_F32) == kda.KDA_ALGO_SIMT
     assert rp(2, 100, 4, dk=64) == kda.KDA_ALGO_SIMT

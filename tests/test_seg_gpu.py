@@ -69,11 +69,12 @@ def test_workspace_size_and_auto_policy():
     nb = kda.kda_seg_workspace_bytes(1, 16, 4)
     assert nb == 1 * 16 * 4 * (2 * 128 * 128 + 128 * 128) * 4
     # the fused path (KDA_ALGO_TC) segments a long single-head batch, not a
-    # wide one; the automatic path takes the two-kernel form for dense
-    # batches (its workspace holds chunk records); packed batches need none
+    # wide one; the automatic path takes the two-kernel form (its workspace
+    # holds chunk records)
     TC = kda.KDA_ALGO_TC
     assert kda.kda_workspace_bytes(1, 1 << 20, 16, 128, 128, algo=TC) > 0
     assert kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=TC) == 0
     assert kda.kda_workspace_bytes(2, 32768, 32, 128, 128) == \
         kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=kda.KDA_ALGO_SPLIT) > 0
-    assert kda.kda_workspace_bytes(1, 1 << 20, 16, 128, 128, packed=1) == 0
+    # packed batches take the two-kernel form too (slices of chunk columns)
+    assert kda.kda_workspace_bytes(1, 1 << 20, 16, 128, 128, packed=1) > 0

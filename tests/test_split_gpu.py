@@ -141,14 +141,8 @@ def test_workspace_too_small_is_refused():
                               2, 128, 128, None, kda.KDA_BF16, 0, 1.0, SPLIT, ws, nb, None,
                               torch.cuda.current_stream())
     assert rc == kda.KDA_ERR_WORKSPACE
-    # a packed batch needs all its chunk records at once
-    cu = torch.tensor([0, 100, 128], dtype=torch.int32, device="cuda")
-    need = kda.kda_workspace_bytes(2, 128, 2, 128, 128, algo=SPLIT, packed=1)
-    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
-    rc = kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], None, out, None, 2, 128,
-                              2, 128, 128, cu, kda.KDA_BF16, 0, 1.0, SPLIT, ws, need - 256, None,
-                              torch.cuda.current_stream())
-    assert rc == kda.KDA_ERR_WORKSPACE
+    # (a packed batch needs at least one chunk column of records:
+    # test_split_packed_workspace_below_one_column_is_refused)
     assert kda.kda_resolve_algo(kda.KDA_BF16, 128, 128, 0, SPLIT) == SPLIT
     assert kda.kda_resolve_algo(kda.KDA_F32, 128, 128, 0, SPLIT) == -1
     assert kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=SPLIT) >= min_ws(2, 32)
@@ -220,22 +214,78 @@ def test_host_pipeline_matches_device(T, s0_std, final):
 
 # ---- packed batches (cu_seqlens): chunk columns of every sequence at once --
 
-def run_packed(x, algo=SPLIT, status=None, workspace=True):
+def run_packed(x, algo=SPLIT, status=None, workspace=True, ws_bytes=None, final=True,
+               inplace=False):
     d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
     N = d["cu_seqlens"].numel() - 1
     T, H = x["T"], x["H"]
     out = torch.empty_like(d["v"])
-    fs = torch.empty(N, H, 128, 128, device="cuda")
+    s0 = d["init_state"]
+    fs = torch.empty(N, H, 128, 128, device="cuda") if final else None
+    if inplace:
+        fs = s0.clone()
+        s0 = fs
     ws, nb = None, 0
     if workspace:
-        nb = kda.kda_workspace_bytes(N, T, H, 128, 128, algo=algo, packed=1)
+        nb = ws_bytes or kda.kda_workspace_bytes(N, T, H, 128, 128, algo=algo, packed=1)
         ws = torch.empty(max(nb, 1), dtype=torch.uint8, device="cuda")
-    rc = kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"], out,
+    rc = kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], s0, out,
                               fs, N, T, H, 128, 128, d["cu_seqlens"], kda.KDA_BF16, 0, 1.0, algo,
                               ws, nb, status, torch.cuda.current_stream())
     assert rc == 0, kda.status_string(rc)
     torch.cuda.synchronize()
-    return out.float().cpu().numpy(), fs.cpu().numpy()
+    return out.float().cpu().numpy(), (fs.cpu().numpy() if fs is not None else None)
+
+
+def packed_min_ws(N, T, H):
+    # [carry][chunk offsets][chunk table][records of one chunk column]
+    def r256(v):
+        return (v + 255) // 256 * 256
+    g_max = (T + 63) // 64 + N
+    return (r256(N * H * 128 * 128 * 4) + r256((N + 1) * 4) + r256(g_max * 8) + H * REC)
+
+
+@pytest.mark.parametrize("extra_cols", [0, 2, 5])
+def test_split_packed_slices_bit_identical(extra_cols):
+    """A packed batch in slices of 1, 3 and 6 chunk columns (the workspace
+    holds that many columns of records): sequences that span slices carry
+    their state across them, empty and one-token sequences pass through;
+    bit-identical to the one-slice run, with and without a final state and
+    with the state updated in place."""
+    lens = (130, 0, 1, 300, 64, 0, 65, 17)
+    w = small_workload("pks", B=1, T=sum(lens), H=2, dk=128, dv=128, seed=43, varlen=True,
+                       lengths=lens, s0_std=0.03)
+    x = make_inputs(w)
+    o1, s1 = run_packed(x)
+    N, T, H = len(lens), sum(lens), 2
+    nb = packed_min_ws(N, T, H) + extra_cols * H * REC
+    o2, s2 = run_packed(x, ws_bytes=nb)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(s1, s2)
+    o3, s3 = run_packed(x, ws_bytes=nb, final=False)
+    assert s3 is None
+    np.testing.assert_array_equal(o1, o3)
+    o4, s4 = run_packed(x, ws_bytes=nb, inplace=True)
+    np.testing.assert_array_equal(o1, o4)
+    np.testing.assert_array_equal(s1, s4)
+    o_ref, s_ref = oracle.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["init_state"],
+                              x["cu_seqlens"])
+    assert rel(o2, o_ref) <= 1e-2 and rel(s2, s_ref) <= 1e-2
+
+
+def test_split_packed_workspace_below_one_column_is_refused():
+    lens = (100, 28)
+    w = small_workload("pkr", B=1, T=sum(lens), H=2, dk=128, dv=128, seed=44, varlen=True,
+                       lengths=lens)
+    x = make_inputs(w)
+    d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+    nb = packed_min_ws(2, sum(lens), 2) - 256
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    rc = kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], None,
+                              torch.empty_like(d["v"]), None, 2, sum(lens), 2, 128, 128,
+                              d["cu_seqlens"], kda.KDA_BF16, 0, 1.0, SPLIT, ws, nb, None,
+                              torch.cuda.current_stream())
+    assert rc == kda.KDA_ERR_WORKSPACE
 
 
 @pytest.mark.parametrize("lens,s0_std", [((100, 64, 0, 1, 257, 130), 0.02),
