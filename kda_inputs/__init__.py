@@ -87,6 +87,12 @@ WORKLOADS = {
                                   beta_mean=2.0, varlen=True),
     "ctx1m": Workload("ctx1m", B=1, T=1 << 20, H=16, dk=128, dv=128, chunk=64,
                       dtype=torch.bfloat16, seed=4, g_mean=-1.0),
+    # a packed 1M-token batch too long to hold every chunk record at once
+    # (slices of chunk columns), with initial states: not one of the five
+    # workloads, a check of the sliced packed path at full size
+    "varlen_ctx1m": Workload("varlen_ctx1m", B=1, T=1 << 20, H=16, dk=128, dv=128, chunk=64,
+                             dtype=torch.bfloat16, seed=5, g_mean=-1.0, s0_std=0.02,
+                             varlen=True, varlen_lo=1024, varlen_hi=65536),
 }
 
 

@@ -248,3 +248,15 @@ def test_full_varlen_floor_hard_sampled():
 
 def test_full_ctx1m_sampled():
     _sampled_check("ctx1m", [(0, 0), (0, 11)])
+
+
+def test_full_varlen_ctx1m_sampled():
+    # 1M tokens packed in ~32 sequences: more chunk records than the default
+    # workspace holds, so the two-kernel path runs in slices of chunk columns
+    # and sequences carry their state across slices
+    w = WORKLOADS["varlen_ctx1m"]
+    assert kda.kda_resolve_path(w.n_seqs(), w.T, w.H, packed=True) == kda.KDA_ALGO_SPLIT
+    g_max = w.T // 64 + w.n_seqs()
+    assert kda.kda_workspace_bytes(w.n_seqs(), w.T, w.H, 128, 128, packed=1) < \
+        g_max * w.H * 66048
+    _sampled_check("varlen_ctx1m", [(0, 9)])
