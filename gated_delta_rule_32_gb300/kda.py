@@ -62,6 +62,9 @@ _SIGS = {
                                                         _vp, _vp]),
     "kda_debug_intra": (_i, [_vp] * 5 + [_i] * 5 + [_vp, _i, _i] + [_vp] * 6 + [_vp]),
     "kda_debug_stall_test": (_i, [_i]),
+    "kda_segment_summary": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _vp]),
+    "kda_summary_floats": (ctypes.c_size_t, [_i] * 4),
+    "kda_state_compose": (_i, [_vp, _i, _vp, _vp] + [_i] * 4 + [_vp]),
     "kda_debug_record_capacity": (_i, [ctypes.c_int64]),
 }
 
@@ -269,3 +272,20 @@ def kda_debug_stall_test(flags: int) -> int:
 def kda_debug_record_capacity(items: int) -> int:
     """Debug builds: the chunk-record capacity the kernels are told (0 = real)."""
     return load().kda_debug_record_capacity(int(items))
+
+
+def kda_segment_summary(q, k, v, g_logit, beta, summary, B, T, H, dk=128, dv=128,
+                        dev_status=None, stream=None) -> int:
+    return load().kda_segment_summary(_p(q), _p(k), _p(v), _p(g_logit), _p(beta),
+                                      _p(summary), B, T, H, dk, dv, _p(dev_status),
+                                      _stream(stream))
+
+
+def kda_summary_floats(N, H, dk=128, dv=128) -> int:
+    return load().kda_summary_floats(N, H, dk, dv)
+
+
+def kda_state_compose(summaries, m, init_state, state_out, N, H, dk=128, dv=128,
+                      stream=None) -> int:
+    return load().kda_state_compose(_p(summaries), m, _p(init_state), _p(state_out), N, H,
+                                    dk, dv, _stream(stream))

@@ -221,6 +221,42 @@ kda_status kda_chunk_fwd_seg_static(const uint16_t* q, const uint16_t* k, const 
                                     int B, int T, int H, int dk, int dv, float scale, int nseg,
                                     int32_t* dev_status, kda_stream_t stream);
 
+/*
+ * Context parallelism: the token axis of a batch split across devices
+ * (Kimi K3 architecture, orkas.ai, "The cost is paid in the serving stack";
+ * Towards AI walkthrough, "Infrastructure co-design": each device's span is
+ * summarised by a cumulative transition and a zero-initialised state, which
+ * compose; a prefix scan over one fixed-size all-gather gives each device
+ * its entry state).
+ *
+ * kda_segment_summary -- the summary of the span [0, T) of every sequence of
+ * a dense bf16 batch (dk = dv = 128; layouts as kda_chunk_fwd): running the
+ * span from a state S_in gives S_out = P S_in + S0.  `summary` (device, fp32,
+ * 16-byte aligned, kda_summary_floats(B, H, dk, dv) floats, not overlapping
+ * the inputs) receives P [B][H][dk][dk] followed by S0 [B][H][dk][dv].  T = 0
+ * gives P = I, S0 = 0.  Asynchronous on `stream`; dev_status as in
+ * kda_chunk_fwd_ex.
+ */
+kda_status kda_segment_summary(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               const uint16_t* g_logit, const uint16_t* beta, float* summary,
+                               int B, int T, int H, int dk, int dv, int32_t* dev_status,
+                               kda_stream_t stream);
+
+/* Floats of one summary: N * H * (dk * dk + dk * dv). */
+size_t kda_summary_floats(int N, int H, int dk, int dv);
+
+/*
+ * kda_state_compose -- the state after m consecutive spans, from their
+ * summaries in order: S = P_{m-1}( ... (P_0 S_init + S0_0) ... ) + S0_{m-1}.
+ * `summaries` (device, fp32) holds the m summaries back to back, each laid
+ * out as kda_segment_summary writes it; init_state [N][H][dk][dv] or NULL
+ * (zero); state_out [N][H][dk][dv] (may equal init_state).  m = 0 copies the
+ * initial state.  dk = dv = 128; fp32 arithmetic.  Asynchronous on `stream`.
+ */
+kda_status kda_state_compose(const float* summaries, int m, const float* init_state,
+                             float* state_out, int N, int H, int dk, int dv,
+                             kda_stream_t stream);
+
 /* Scratch bytes of kda_chunk_fwd_seg (0 when nseg < 2). */
 size_t kda_seg_workspace_bytes(int B, int H, int nseg, int dk, int dv);
 
