@@ -175,10 +175,11 @@ class ClockSampler:
                 "samples": len(rows), "reasons": reasons}
 
 
-def oracle_sample(w, n_units: int, tokens: int, threads: int = 0):
+def oracle_sample(w, n_units: int, tokens: int, threads: int = 0, min_seconds: float = 0.0):
     """Time the fp64 oracle on the first n_units (row, head) units of the
-    workload, first `tokens` tokens each.  Returns (seconds, token-heads,
-    threads used)."""
+    workload, first `tokens` tokens each, repeated (inputs drawn once) until
+    at least `min_seconds` of oracle time have passed.  Returns (seconds,
+    token-heads, threads used), summed over the repetitions."""
     import oracle
     units = [(b, h) for b in range(w.B) for h in range(w.H)][:n_units]
     T = min(tokens, w.T)
@@ -204,10 +205,13 @@ def oracle_sample(w, n_units: int, tokens: int, threads: int = 0):
             cu.append(T)
         cu = np.array(cu, dtype=np.int32)
         s0 = None
-    t0 = time.perf_counter()
-    _, _, used = oracle.fwd(q, k, v, g, beta, s0, cu, nthreads=threads, return_threads=True)
-    dt = time.perf_counter() - t0
-    return dt, len(units) * T, used
+    dt, reps = 0.0, 0
+    while reps == 0 or dt < min_seconds:
+        t0 = time.perf_counter()
+        _, _, used = oracle.fwd(q, k, v, g, beta, s0, cu, nthreads=threads, return_threads=True)
+        dt += time.perf_counter() - t0
+        reps += 1
+    return dt, reps * len(units) * T, used
 
 
 def resolve_workload(args):
@@ -440,11 +444,13 @@ def run_ours(args):
                            "frac": alg_flops(w) / (kernel_ms / 1e3) / 1e12 / bf16_tf}}
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and ws == 1:
-        dt, th, used = oracle_sample(w, args.cpu_units, args.cpu_tokens)
+        dt, th, used = oracle_sample(w, args.cpu_units, args.cpu_tokens,
+                                     min_seconds=args.cpu_seconds)
+        n_u, n_t = min(args.cpu_units, w.B * w.H), min(args.cpu_tokens, w.T)
         cpu = {"value": th / w.H / dt, "unit": "tokens/s", "cores": used, "kind": "oracle",
-               "sample": "%d (row, head) units x first %d tokens (of %d heads x %d tokens)"
-                         % (min(args.cpu_units, w.B * w.H), min(args.cpu_tokens, w.T),
-                            w.B * w.H, w.T),
+               "sample": "%d (row, head) units x first %d tokens (of %d heads x %d tokens), "
+                         "repeated %d times (%.1f s of oracle time)"
+                         % (n_u, n_t, w.B * w.H, w.T, th // (n_u * n_t), dt),
                "seconds": dt}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -479,7 +485,9 @@ def main():
     ap.add_argument("--T", type=int, default=0, help="resize (profiling captures only)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-units", type=int, default=16)
+    ap.add_argument("--cpu-units", type=int, default=64)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="oracle time the CPU baseline accumulates")
     ap.add_argument("--cpu-tokens", type=int, default=32768)
     ap.add_argument("--ref-units", type=int, default=16)
     ap.add_argument("--ref-tokens", type=int, default=4096)
