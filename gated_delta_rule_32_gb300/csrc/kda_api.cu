@@ -4,9 +4,11 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "kda_common.cuh"
 
@@ -159,12 +161,19 @@ size_t kda_split_min_workspace_bytes(int N, int H);
 kda_status kda_run_split_range(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
                                cudaStream_t stream, int c0, int cnt);
 size_t kda_split_slice_workspace_bytes(int N, int H, int chunks);
+kda_status kda_run_split_packed_range(const kda::FwdParams& p, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream, int g0,
+                                      int cnt, bool prepare);
+int kda_split_packed_g_max(int N, int T);
+size_t kda_split_packed_slice_workspace_bytes(int N, int T, int H, int cols);
 
 namespace {
-// The end-to-end call on the two-kernel path runs the sequence in pieces of
-// whole chunks: the inputs of piece i + 1 go to the device on two copy
-// streams while piece i runs on the caller's stream and the output of piece
-// i - 1 comes back on a third, so the host link, not the sum of copies and
+// The end-to-end call on the two-kernel path runs the batch in pieces of
+// whole chunks (a dense batch: chunks [c0, c1) of every sequence; a packed
+// one: chunk columns [g0, g1), which are one contiguous range of token
+// rows): the inputs of piece i + 1 go to the device on two copy streams
+// while piece i runs on the caller's stream and the output of piece i - 1
+// comes back on a third, so the host link, not the sum of copies and
 // kernels, sets the time.  The state crosses pieces exactly as it crosses
 // slices (fp32, unchanged), so the result does not depend on the cut.
 constexpr int kHostPieces = 8;
@@ -173,8 +182,21 @@ int host_piece_chunks(int T) {
   const int pieces = nchunks < kHostPieces ? nchunks : kHostPieces;
   return (nchunks + pieces - 1) / pieces;
 }
-bool host_pipelined(int dtype, int dk, int dv, int packed, int T) {
-  return !packed && use_split(dtype, dk, dv, 0, KDA_ALGO_AUTO, 0, 1, T, 1) && (T + 63) / 64 >= 2;
+// chunk columns per piece of a packed batch (of the bound ceil(T / 64) + N)
+int host_piece_cols(int N, int T) {
+  const int g = kda_split_packed_g_max(N, T);
+  const int pieces = g < kHostPieces ? g : kHostPieces;
+  return (g + pieces - 1) / pieces;
+}
+bool host_pipelined(int dtype, int dk, int dv, int packed, int N, int T) {
+  if (packed)
+    return use_split(dtype, dk, dv, 0, KDA_ALGO_AUTO, 1, N, T, 1) &&
+           kda_split_packed_g_max(N, T) >= 2;
+  return use_split(dtype, dk, dv, 0, KDA_ALGO_AUTO, 0, 1, T, 1) && (T + 63) / 64 >= 2;
+}
+size_t host_piece_workspace_bytes(int N, int T, int H, int packed) {
+  return packed ? kda_split_packed_slice_workspace_bytes(N, T, H, host_piece_cols(N, T))
+                : kda_split_slice_workspace_bytes(N, H, host_piece_chunks(T));
 }
 }  // namespace
 // A workspace smaller than the default (but at least the minimum) runs the
@@ -397,8 +419,8 @@ size_t kda_host_staging_bytes(int B, int T, int H, int dk, int dv, int dtype, in
   // the path's own workspace (chunk records of one piece of the two-kernel
   // form, or the segment scratch), so that the end-to-end call allocates
   // nothing itself
-  if (host_pipelined(dtype, dk, dv, packed, T))
-    tot += round_up(kda_split_slice_workspace_bytes(B, H, host_piece_chunks(T)));
+  if (host_pipelined(dtype, dk, dv, packed, B, T))
+    tot += round_up(host_piece_workspace_bytes(B, T, H, packed));
   else
     tot += round_up(kda_workspace_bytes(B, T, H, dk, dv, dtype, 0, KDA_ALGO_AUTO, packed));
   return tot;
@@ -496,6 +518,117 @@ kda_status host_pipelined_run(const void* q, const void* k, const void* v, const
   if (st == KDA_OK && hstat != 0) st = (kda_status)hstat;
   return st;
 }
+
+// The pieces of a pipelined end-to-end call on a packed batch: chunk columns
+// [g0, g0 + per) of the bound ceil(T / 64) + N, each a contiguous range of
+// token rows [row(g0), row(g0 + per)).  A piece's kernels also read up to 63
+// rows past its range (the tile of a sequence's last, short chunk; those
+// rows enter with zero weight), so each piece's copy reaches 64 rows
+// further, and every row is copied once.  cu_seqlens: host offsets, already
+// checked.
+kda_status host_pipelined_packed_run(const void* q, const void* k, const void* v,
+                                     const void* g_logit, const void* beta,
+                                     const float* init_state, void* out, float* final_state,
+                                     int N, int T, int H, float scale, const int32_t* cu,
+                                     char* dq, char* dk_, char* dv_, char* dg, char* db,
+                                     float* ds0, char* dout, float* ds1, int32_t* dcu,
+                                     int32_t* dstat, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream) {
+  constexpr int D = 128;
+  const size_t row_qk = (size_t)H * D * 2, row_b = (size_t)H * 2;  // bytes per token row
+  // first column of each sequence (ceil(len / 64) columns each)
+  std::vector<int64_t> off(N + 1, 0);
+  for (int n = 0; n < N; ++n) off[n + 1] = off[n] + (cu[n + 1] - cu[n] + 63) / 64;
+  const int64_t cols = off[N];
+  auto row_of = [&](int64_t g) -> int64_t {  // first token row of column g
+    if (g >= cols) return T;
+    const int n = (int)(std::upper_bound(off.begin(), off.end(), g) - off.begin()) - 1;
+    return cu[n] + 64 * (g - off[n]);
+  };
+  const int g_max = kda_split_packed_g_max(N, T), per = host_piece_cols(N, T);
+  const int pieces = (g_max + per - 1) / per;
+  cudaStream_t s_in[2] = {nullptr, nullptr}, s_out = nullptr;
+  cudaEvent_t ev0 = nullptr, ev_in[2][kHostPieces] = {}, ev_c[kHostPieces] = {};
+  kda_status st = KDA_OK;
+  auto cu_ok = [&](cudaError_t e) {
+    if (e != cudaSuccess && st == KDA_OK) st = KDA_ERR_CUDA;
+    return st == KDA_OK;
+  };
+  cu_ok(cudaStreamCreateWithFlags(&s_in[0], cudaStreamNonBlocking));
+  cu_ok(cudaStreamCreateWithFlags(&s_in[1], cudaStreamNonBlocking));
+  cu_ok(cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking));
+  cu_ok(cudaEventCreateWithFlags(&ev0, cudaEventDisableTiming));
+  for (int i = 0; i < pieces; ++i) {
+    cu_ok(cudaEventCreateWithFlags(&ev_in[0][i], cudaEventDisableTiming));
+    cu_ok(cudaEventCreateWithFlags(&ev_in[1][i], cudaEventDisableTiming));
+    cu_ok(cudaEventCreateWithFlags(&ev_c[i], cudaEventDisableTiming));
+  }
+  int32_t hstat = 0;
+  if (st == KDA_OK) {
+    kda::FwdParams p{};
+    p.q = dq; p.k = dk_; p.v = dv_; p.g = dg; p.beta = db;
+    p.init_state = ds0; p.out = dout; p.final_state = ds1; p.dev_status = dstat;
+    p.cu_seqlens = dcu;
+    p.N = N; p.T = T; p.H = H; p.dk = D; p.dv = D; p.scale = scale;
+    // the offsets and status word on the caller's stream, ahead of the
+    // first piece's chunk table
+    cu_ok(cudaMemcpyAsync(dcu, cu, (size_t)(N + 1) * sizeof(int32_t), cudaMemcpyHostToDevice,
+                          stream));
+    cu_ok(cudaMemsetAsync(dstat, 0, sizeof(int32_t), stream));
+    cu_ok(cudaEventRecord(ev0, stream));
+    cu_ok(cudaStreamWaitEvent(s_in[0], ev0, 0));
+    cu_ok(cudaStreamWaitEvent(s_in[1], ev0, 0));
+    auto h2d = [&](char* dst, const void* src, size_t off_b, size_t n, cudaStream_t sm) {
+      return cu_ok(cudaMemcpyAsync(dst + off_b, static_cast<const char*>(src) + off_b, n,
+                                   cudaMemcpyHostToDevice, sm));
+    };
+    int64_t copied = 0;  // rows [0, copied) are on the device or queued
+    for (int i = 0; i < pieces && st == KDA_OK; ++i) {
+      const int g0 = i * per, cnt = g_max - g0 < per ? g_max - g0 : per;
+      const int64_t r0 = row_of(g0), r1 = row_of((int64_t)g0 + cnt);
+      const int64_t need = r1 + 64 < T ? r1 + 64 : T;
+      if (need > copied) {
+        const size_t a = (size_t)copied, nr = (size_t)(need - copied);
+        h2d(dq, q, a * row_qk, nr * row_qk, s_in[0]);
+        h2d(dk_, k, a * row_qk, nr * row_qk, s_in[0]);
+        h2d(dg, g_logit, a * row_qk, nr * row_qk, s_in[1]);
+        h2d(dv_, v, a * row_qk, nr * row_qk, s_in[1]);
+        h2d(db, beta, a * row_b, nr * row_b, s_in[1]);
+        copied = need;
+      }
+      if (i == 0 && ds0)
+        h2d(reinterpret_cast<char*>(ds0), init_state, 0, (size_t)N * H * D * D * 4, s_in[0]);
+      cu_ok(cudaEventRecord(ev_in[0][i], s_in[0]));
+      cu_ok(cudaEventRecord(ev_in[1][i], s_in[1]));
+      cu_ok(cudaStreamWaitEvent(stream, ev_in[0][i], 0));
+      cu_ok(cudaStreamWaitEvent(stream, ev_in[1][i], 0));
+      if (st == KDA_OK) st = kda_run_split_packed_range(p, ws, ws_bytes, stream, g0, cnt, i == 0);
+      cu_ok(cudaEventRecord(ev_c[i], stream));
+      cu_ok(cudaStreamWaitEvent(s_out, ev_c[i], 0));
+      if (r1 > r0)
+        cu_ok(cudaMemcpyAsync(static_cast<char*>(out) + (size_t)r0 * row_qk,
+                              dout + (size_t)r0 * row_qk, (size_t)(r1 - r0) * row_qk,
+                              cudaMemcpyDeviceToHost, s_out));
+    }
+    if (ds1)
+      cu_ok(cudaMemcpyAsync(final_state, ds1, (size_t)N * H * D * D * 4, cudaMemcpyDeviceToHost,
+                            s_out));
+    cu_ok(cudaMemcpyAsync(&hstat, dstat, sizeof(int32_t), cudaMemcpyDeviceToHost, s_out));
+  }
+  // everything queued is waited for, whatever failed
+  for (cudaStream_t sm : {s_in[0], s_in[1], s_out, stream})
+    if (sm || sm == stream) cu_ok(cudaStreamSynchronize(sm));
+  for (int i = 0; i < pieces; ++i) {
+    if (ev_in[0][i]) cudaEventDestroy(ev_in[0][i]);
+    if (ev_in[1][i]) cudaEventDestroy(ev_in[1][i]);
+    if (ev_c[i]) cudaEventDestroy(ev_c[i]);
+  }
+  if (ev0) cudaEventDestroy(ev0);
+  for (cudaStream_t sm : {s_in[0], s_in[1], s_out})
+    if (sm) cudaStreamDestroy(sm);
+  if (st == KDA_OK && hstat != 0) st = (kda_status)hstat;
+  return st;
+}
 }  // namespace
 
 extern "C" {
@@ -536,15 +669,19 @@ kda_status kda_chunk_fwd_host(const void* q, const void* k, const void* v, const
   float* ds1 = final_state ? (float*)take(s.state) : nullptr;
   int32_t* dcu = packed ? (int32_t*)take(s.cu) : nullptr;
   int32_t* dstat = (int32_t*)take(sizeof(int32_t));
-  const bool piped = host_pipelined(dtype, dk, dv, packed, T);
+  const bool piped = host_pipelined(dtype, dk, dv, packed, B, T);
   const size_t ws_bytes =
-      piped ? kda_split_slice_workspace_bytes(B, H, host_piece_chunks(T))
+      piped ? host_piece_workspace_bytes(B, T, H, packed)
             : kda_workspace_bytes(B, T, H, dk, dv, dtype, 0, KDA_ALGO_AUTO, packed);
   void* ws = ws_bytes ? take(ws_bytes) : nullptr;
   if (piped) {
-    kda_status st = host_pipelined_run(q, k, v, g_logit, beta, init_state, out, final_state, B,
-                                       T, H, scale, dq, dk_, dv_, dg, db, ds0, dout, ds1, dstat,
-                                       ws, ws_bytes, stream);
+    kda_status st =
+        packed ? host_pipelined_packed_run(q, k, v, g_logit, beta, init_state, out, final_state,
+                                           B, T, H, scale, cu_seqlens, dq, dk_, dv_, dg, db, ds0,
+                                           dout, ds1, dcu, dstat, ws, ws_bytes, stream)
+               : host_pipelined_run(q, k, v, g_logit, beta, init_state, out, final_state, B, T,
+                                    H, scale, dq, dk_, dv_, dg, db, ds0, dout, ds1, dstat, ws,
+                                    ws_bytes, stream);
     if (owned) cudaFreeAsync(base, stream);
     if (cudaStreamSynchronize(stream) != cudaSuccess && st == KDA_OK) st = KDA_ERR_CUDA;
     return st;

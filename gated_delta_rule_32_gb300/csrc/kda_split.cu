@@ -1392,46 +1392,57 @@ kda_status run_overlapped(const kda::FwdParams& p, const SplitPlan& pl, int slic
   return st;
 }
 
-// The slices run back to back on `stream`; `one_slice` refuses a workspace
-// that would need more than one slice.
-// A packed batch: its chunk table, then both kernels over each slice of
-// chunk columns in turn (one slice when the workspace holds every column).
-kda_status launch_packed(const kda::FwdParams& p, const SplitPlan& pl, cudaStream_t stream) {
+// A packed batch's chunk table: the sequences' chunk offsets, then the first
+// row and row count of every column.
+kda_status packed_prepare(const kda::FwdParams& p, const SplitPlan& pl, cudaStream_t stream) {
   kda_split_offsets_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.N, p.T, pl.chunk_off,
                                                    p.dev_status);
   const int tb_need = (pl.g_max + 255) / 256;
   const int tb = tb_need < 8 * pl.sms ? tb_need : 8 * pl.sms;
   kda_split_table_kernel<<<tb, 256, 0, stream>>>(p.cu_seqlens, pl.chunk_off, p.N, pl.g_max,
                                                  pl.chunk_tab);
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+// Both kernels over chunk columns [g0, g0 + cnt) of a packed batch (after
+// packed_prepare), the records at the start of the workspace's record area.
+kda_status packed_slice(const kda::FwdParams& p, const SplitPlan& pl, int g0, int cnt,
+                      cudaStream_t stream) {
+  SplitParams sp;
+  sp.p = p;
+  sp.rec = pl.rec;
+  sp.c_begin = 0;
+  sp.c_count = 0;
+  // sequences start from init_state and end in final_state; one that
+  // spans slices carries its state through final_state or the workspace
+  sp.s_in = pl.through;
+  sp.s_out = pl.through;
+  sp.chunk_tab = pl.chunk_tab;
+  sp.chunk_off = pl.chunk_off;
+  sp.g_max = pl.g_max;
+  sp.g_begin = g0;
+  sp.g_count = cnt;
+  sp.stall_test = g_stall_test.load();
+  sp.rec_items = told_capacity((int64_t)cnt * p.H);
+  sp.rows = p.T;
+  const int64_t items = (int64_t)cnt * p.H;
+  const int grid = items < 2 * (int64_t)pl.sms ? (int)items : 2 * pl.sms;
+  kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, sp);
   if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-  const int fit = pl.fit < (size_t)pl.g_max ? (int)pl.fit : pl.g_max;
-  for (int g0 = 0; g0 < pl.g_max; g0 += fit) {
-    const int cnt = pl.g_max - g0 < fit ? pl.g_max - g0 : fit;
-    SplitParams sp;
-    sp.p = p;
-    sp.rec = pl.rec;
-    sp.c_begin = 0;
-    sp.c_count = 0;
-    // sequences start from init_state and end in final_state; one that
-    // spans slices carries its state through final_state or the workspace
-    sp.s_in = pl.through;
-    sp.s_out = pl.through;
-    sp.chunk_tab = pl.chunk_tab;
-    sp.chunk_off = pl.chunk_off;
-    sp.g_max = pl.g_max;
-    sp.g_begin = g0;
-    sp.g_count = cnt;
-    sp.stall_test = g_stall_test.load();
-    sp.rec_items = told_capacity((int64_t)cnt * p.H);
-    sp.rows = p.T;
-    const int64_t items = (int64_t)cnt * p.H;
-    const int grid = items < 2 * (int64_t)pl.sms ? (int)items : 2 * pl.sms;
-    kda_tc_intra_kernel<<<grid, kThreads, I_SMEM, stream>>>(pl.mq, pl.mk, pl.mg, sp);
-    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-    kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(pl.mv, sp);
-    if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
-  }
+  kda_tc_state_kernel<<<dim3(2, p.H, p.N), kThreads, S_SMEM, stream>>>(pl.mv, sp);
+  if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   return KDA_OK;
+}
+
+// The slices run back to back on `stream`.
+// A packed batch: its chunk table, then both kernels over each slice of
+// chunk columns in turn (one slice when the workspace holds every column).
+kda_status launch_packed(const kda::FwdParams& p, const SplitPlan& pl, cudaStream_t stream) {
+  kda_status st = packed_prepare(p, pl, stream);
+  const int fit = pl.fit < (size_t)pl.g_max ? (int)pl.fit : pl.g_max;
+  for (int g0 = 0; g0 < pl.g_max && st == KDA_OK; g0 += fit)
+    st = packed_slice(p, pl, g0, pl.g_max - g0 < fit ? pl.g_max - g0 : fit, stream);
+  return st;
 }
 
 kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
@@ -1474,6 +1485,34 @@ kda_status kda_run_split_range(const kda::FwdParams& p, void* workspace, size_t 
   if (st != KDA_OK) return st;
   if (c0 < 0 || cnt < 1 || c0 + cnt > pl.nchunks || (size_t)cnt > pl.fit) return KDA_ERR_INVALID_ARG;
   return launch_slice(p, pl, c0, cnt, stream, stream, 3, pl.rec, 2 * pl.sms);
+}
+
+// Chunk columns [g0, g0 + cnt) of a packed batch alone (both kernels), the
+// chunk table built first when `prepare` is set (the first range of a call).
+// Sequences enter from init_state where they start, else from the state the
+// previous range left in final_state or the workspace; the workspace must
+// hold cnt columns of records.
+kda_status kda_run_split_packed_range(const kda::FwdParams& p, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream, int g0,
+                                      int cnt, bool prepare) {
+  if (!p.cu_seqlens) return KDA_ERR_UNSUPPORTED;
+  SplitPlan pl;
+  kda_status st = plan_split(p, workspace, workspace_bytes, pl);
+  if (st != KDA_OK) return st;
+  if (g0 < 0 || cnt < 1 || g0 + cnt > pl.g_max || (size_t)cnt > pl.fit)
+    return KDA_ERR_INVALID_ARG;
+  if (prepare && (st = packed_prepare(p, pl, stream)) != KDA_OK) return st;
+  return packed_slice(p, pl, g0, cnt, stream);
+}
+
+// Chunk columns of a packed batch: an upper bound, ceil(T / 64) + N.
+int kda_split_packed_g_max(int N, int T) { return packed_g_max(N, T); }
+
+// Device bytes of the two-kernel path for a packed batch run `cols` chunk
+// columns at a time.
+size_t kda_split_packed_slice_workspace_bytes(int N, int T, int H, int cols) {
+  if (N < 1 || H < 1 || T < 1 || cols < 1) return 0;
+  return packed_layout(N, T, H, cols).total;
 }
 
 // Device bytes of the two-kernel path for slices of `chunks` chunks.

@@ -273,12 +273,16 @@ size_t kda_workspace_bytes(int N, int T, int H, int dk, int dv, int dtype, int c
  * pointer here is a host pointer.  dev_buffer: device memory of at least
  * kda_host_staging_bytes() bytes, or NULL (then taken from and returned to
  * the stream-ordered allocator).  The device status is read back and
- * returned as the call's result.  On the two-kernel path (dense bf16,
- * dk = dv = 128, two or more chunks) the call runs in up to eight pieces of
- * whole chunks: while piece i runs on `stream`, the inputs of piece i + 1 are
- * copied in and the output of piece i - 1 copied out on streams of the
- * call's own, so the copies overlap the kernels; the result is bit-identical
- * to kda_chunk_fwd_ex on device copies of the same inputs.
+ * returned as the call's result.  On the two-kernel path (bf16, dk = dv =
+ * 128, two or more chunks, or for a packed batch two or more columns of
+ * the bound ceil(T / 64) + B) the call runs in up to eight pieces of whole
+ * chunks -- chunks [c0, c1) of every sequence of a dense batch, or chunk
+ * columns [g0, g1) of a packed one (a contiguous range of token rows):
+ * while piece i runs on `stream`, the inputs of piece i + 1 are copied in
+ * and the output of piece i - 1 copied out on streams of the call's own,
+ * so the copies overlap the kernels; the result is bit-identical to
+ * kda_chunk_fwd_ex on device copies of the same inputs.  cu_seqlens is a
+ * host array here; it is checked before any copy.
  */
 kda_status kda_chunk_fwd_host(const void* q, const void* k, const void* v, const void* g_logit,
                               const void* beta, const float* init_state, void* out,

@@ -26,8 +26,12 @@ def main():
     ms = 10.0 + 5.0 * rank          # this rank's step time
     slowest = bench.max_over_ranks(ms, ws, torch.device("cpu"))
     value = bench.job_value(ws, w.B * w.T, slowest)
-    print(json.dumps({"rank": rank, "ws": ws, "seed": w.seed, "slowest_ms": slowest,
-                      "value": value, "q0": float(x["q"].flatten()[0])}), flush=True)
+    # one write per line: the ranks share the pipe, and print() may write
+    # the text and its newline separately when the stream is unbuffered
+    line = json.dumps({"rank": rank, "ws": ws, "seed": w.seed, "slowest_ms": slowest,
+                       "value": value, "q0": float(x["q"].flatten()[0])})
+    sys.stdout.write(line + "\n")
+    sys.stdout.flush()
     dist.barrier()
     dist.destroy_process_group()
 

@@ -108,6 +108,23 @@ def test_staging_bytes_of_the_pipelined_host_call(lib):
         r256(kda.kda_workspace_bytes(B, 64, H, 128, 128))
 
 
+
+def test_staging_bytes_of_the_pipelined_packed_host_call(lib):
+    # a packed bf16 batch at dk = dv = 128 runs in up to eight pieces of chunk
+    # columns (of the bound ceil(T / 64) + N): the staging holds the inputs,
+    # outputs, states and offsets plus the packed workspace of one piece
+    def r256(x):
+        return (x + 255) // 256 * 256
+    N, T, H = 28, 1 << 20, 16
+    qk = T * H * 128 * 2
+    state = N * H * 128 * 128 * 4
+    fixed = 5 * r256(qk) + r256(T * H * 2) + 2 * r256(state) + r256((N + 1) * 4) + 256
+    g_max = (T + 63) // 64 + N
+    per = (g_max + 7) // 8
+    piece = r256(state) + r256((N + 1) * 4) + r256(g_max * 8) + per * H * 66048
+    n = kda.kda_host_staging_bytes(N, T, H, 128, 128, kda.KDA_BF16, 1, 1, 1)
+    assert n == fixed + r256(piece)
+
 def test_package_fails_loudly_without_library(tmp_path):
     saved = kda._lib
     try:

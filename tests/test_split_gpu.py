@@ -273,6 +273,38 @@ def test_split_packed_slices_bit_identical(extra_cols):
     assert rel(o2, o_ref) <= 1e-2 and rel(s2, s_ref) <= 1e-2
 
 
+@pytest.mark.parametrize("lens,s0_std,final", [
+    ((130, 0, 1, 300, 64, 0, 65, 17), 0.03, True),   # 18 column bound: 6 pieces of 3
+    ((1000,), 0.0, True),                            # one sequence across every piece
+    ((5, 7, 0, 3, 1, 2), 0.02, False),               # one column per piece, the last empty
+])
+def test_host_pipeline_packed_matches_device(lens, s0_std, final):
+    """kda_chunk_fwd_host on a packed batch runs the two-kernel path in
+    pieces of chunk columns (contiguous token rows, copied in while the
+    previous piece runs, each copy reaching 64 rows past its piece for the
+    tile of a short last chunk): bit-identical to the one-call device run."""
+    N, T, H = len(lens), sum(lens), 2
+    w = small_workload("hostpk", B=1, T=T, H=H, dk=128, dv=128, seed=47, varlen=True,
+                       lengths=lens, s0_std=s0_std)
+    x = make_inputs(w)
+    o_dev, s_dev = run_packed(x, final=final)
+    pin = {k: (v.pin_memory() if torch.is_tensor(v) and k != "cu_seqlens" else v)
+           for k, v in x.items()}
+    out = torch.empty(1, T, H, 128, dtype=torch.bfloat16).pin_memory()
+    fs = torch.empty(N, H, 128, 128).pin_memory() if final else None
+    nb = kda.kda_host_staging_bytes(N, T, H, 128, 128, kda.KDA_BF16,
+                                    int(x["init_state"] is not None), int(final), 1)
+    staging = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    rc = kda.kda_chunk_fwd_host(pin["q"], pin["k"], pin["v"], pin["g"], pin["beta"],
+                                pin["init_state"], out, fs, N, T, H, 128, 128,
+                                x["cu_seqlens"], kda.KDA_BF16, 1.0, staging, nb,
+                                torch.cuda.current_stream())
+    assert rc == 0, kda.status_string(rc)
+    np.testing.assert_array_equal(out.float().numpy(), o_dev)
+    if final:
+        np.testing.assert_array_equal(fs.numpy(), s_dev)
+
+
 def test_split_packed_workspace_below_one_column_is_refused():
     lens = (100, 28)
     w = small_workload("pkr", B=1, T=sum(lens), H=2, dk=128, dv=128, seed=44, varlen=True,
