@@ -92,6 +92,22 @@ struct SplitParams {
   // wait, bit 1 the state kernel's first wait, wait on a barrier that nothing
   // ever completes, with a 1 ms limit, so that the timeout and abort path runs
   int stall_test;
+  // segments of a dense batch (seg_g > 1; records of every chunk at hand):
+  // sequence n is cut into seg_g segments of seg_len chunks (the last one
+  // shorter), state grid z = n * seg_g + segment.  seg_pass 1: segment 0 in
+  // full (from init_state, its final state into seg_entry[n][1]); segments
+  // 1 .. seg_g - 2 from a zero state (final into seg_s0) and their
+  // cumulative transitions (grid x = 2, 3: the state run from the identity
+  // with U = 0, final into seg_trans).  seg_pass 2: segments 1 .. seg_g - 1
+  // in full from seg_entry (the last one's final state into final_state).
+  // Buffers [N][seg_g][H][DK][DV] (seg_trans: [DK][DK]).
+  int seg_g, seg_len, seg_pass;
+  // dense records laid out for every chunk of a sequence (record of chunk c
+  // at (n * H + h) * rec_stride + c) instead of for the slice; 0: the slice
+  int rec_stride;
+  float* seg_entry;
+  float* seg_s0;
+  float* seg_trans;
 };
 
 // limit of the waits the stall test makes run out
@@ -180,7 +196,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int64_t cs = ((int64_t)sp.c_begin + it.cl) * C;
       it.L = (p.T - cs) < C ? (int)(p.T - cs) : C;
       it.row0 = (int64_t)it.n * p.T + cs;
-      it.ri = it.w;
+      it.ri = sp.rec_stride > 0
+                  ? ((int64_t)it.n * H + it.h) * sp.rec_stride + sp.c_begin + it.cl
+                  : it.w;
     }
   };
   // the coordinates of item w (divisions: once per CTA), and those of the
@@ -720,7 +738,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) unsigned char smem[];
   const kda::FwdParams& p = sp.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int half = blockIdx.x, h = blockIdx.y, n = blockIdx.z, H = p.H;
+  const int seg_g = sp.seg_g > 1 ? sp.seg_g : 1;
+  const int half = blockIdx.x & 1, h = blockIdx.y, n = blockIdx.z, H = p.H;
+  // segments: pass 1 grid x = [segment 0: 2 halves][segments 1 .. G - 2:
+  // (state run, transition run) x 2 halves], pass 2 grid x = [segments
+  // 1 .. G - 1: 2 halves].  A transition run starts from the identity, with
+  // U = 0 and no output.
+  int seg = 0;
+  bool trans = false;
+  if (seg_g > 1) {
+    if (sp.seg_pass == 1) {
+      if (blockIdx.x >= 2) {
+        seg = 1 + (int)((blockIdx.x - 2) >> 2);
+        trans = (((blockIdx.x - 2) >> 1) & 1) != 0;
+      }
+    } else {
+      seg = 1 + (int)(blockIdx.x >> 1);
+    }
+  }
 #ifdef KDA_PHASE_TIMING
   long long t_mark = clock64();
   const bool mk = tid == 0 && half == 0 && h == 0 && n == 0;
@@ -734,6 +769,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float* s_in = sp.s_in;
   float* s_out = sp.s_out;
   bool involved = true;  // false: the sequence has nothing in this slice
+  bool emit = true;      // output rows written
+  int64_t in_base = ((int64_t)n * H + h) * (int64_t)DK * DV + half * 64;
+  int64_t out_base = in_base;
   if (sp.chunk_tab) {
     const int c_lo = sp.chunk_off[n], c_hi = sp.chunk_off[n + 1];
     const int g0 = sp.g_begin, g1 = sp.g_begin + sp.g_count;
@@ -753,8 +791,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     row_base = (int64_t)n * p.T;
     seq_len = p.T;
     rec0 = sp.rec + ((int64_t)n * H + h) * (int64_t)sp.c_count * REC_BYTES;
+    if (seg_g > 1) {
+      // this segment's chunks, and where its state enters and leaves
+      const int lo = seg * sp.seg_len, hi = lo + sp.seg_len < sp.c_count ? lo + sp.seg_len
+                                                                          : sp.c_count;
+      nc = hi > lo ? hi - lo : 0;
+      c_first = lo;
+      rec0 += (int64_t)lo * REC_BYTES;
+      const int64_t seg_base =
+          (((int64_t)n * seg_g + seg) * H + h) * (int64_t)DK * DV + half * 64;
+      const int64_t next_base = seg_base + (int64_t)H * DK * DV;  // segment seg + 1
+      if (sp.seg_pass == 1 && seg == 0) {   // segment 0 in full
+        s_in = p.init_state;
+        s_out = sp.seg_entry;
+        out_base = next_base;
+      } else if (sp.seg_pass == 1) {        // zero start (identity: below)
+        s_in = nullptr;
+        s_out = trans ? sp.seg_trans : sp.seg_s0;
+        out_base = seg_base;
+        emit = false;
+      } else {                              // from its entry state, in full
+        s_in = sp.seg_entry;
+        in_base = seg_base;
+        s_out = seg == seg_g - 1 ? p.final_state : nullptr;
+      }
+    }
   }
-  const int64_t sbase = ((int64_t)n * H + h) * (int64_t)DK * DV + half * 64;
   // debug build: this chain's records and rows inside their buffers, else it
   // does nothing but report (every thread takes the same decision)
   bool dbg_bad = false;
@@ -806,14 +868,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t lane_q = 32u * (warp & 3);
   if (dbg_bad && tid == 0 && p.dev_status) atomicExch(p.dev_status, (int32_t)KDA_ERR_BOUNDS);
 
-  // entry state into TMEM (lane = key channel)
+  // entry state into TMEM (lane = key channel); a transition run starts
+  // from the identity's columns half * 64 ..
   if (warp < 4) {
     const int i = tid;
     for (int c = 0; c < 64; c += 16) {
       uint32_t r[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e)
-        r[e] = __float_as_uint(s_in && involved ? s_in[sbase + (int64_t)i * DV + c + e] : 0.0f);
+        r[e] = __float_as_uint(s_in && involved ? s_in[in_base + (int64_t)i * DV + c + e]
+                               : (trans && i == half * 64 + c + e) ? 1.0f : 0.0f);
       sm100::tmem_st16(sm100::taddr(tmem, lane_q, TM_S + c), r);
     }
     sm100::tmem_wait_st();
@@ -882,8 +946,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       landed = c + 1;
       // U = [T Diag(beta); -] V of this half, while the CUDA cores copy S
-      // (the P product's commit covers it)
-      if (tid == 0) {
+      // (the P product's commit covers it); a transition run has U = 0
+      if (tid == 0 && !trans) {
         const uint32_t idu = sm100::idesc_bf16(128, 64, 0, 1);
         const uint32_t s_t = sm100::smem_u32(st + ST_T);
         const uint32_t s_v = sm100::smem_u32(st + ST_V);
@@ -943,7 +1007,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mma_pending = true;
     // output rows of the previous chunk while the tensor cores work on P
-    if (warp >= 6 && c > 0) write_out(c - 1);
+    if (emit && warp >= 6 && c > 0) write_out(c - 1);
     wait_mma();
     SPLIT_MARK(19, mk);
 
@@ -958,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_U + cb + c16), u);
         sm100::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) d[c16 + e] = u[e] - v[e];
+        for (int e = 0; e < 16; ++e) d[c16 + e] = trans ? -v[e] : u[e] - v[e];
       }
 #pragma unroll
       for (int g = 0; g < 4; ++g)
@@ -1000,7 +1064,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (5) state checkpoint (all warps: lane = key channel, the 32 columns
     //     this warp rescales next, so program order alone keeps the read
     //     ahead of the next chunk's rescaling)
-    if (p.ckpt) {
+    if (p.ckpt && emit) {
       const int64_t cs = ((int64_t)c_first + c) * C;
       const int L = (seq_len - cs) < C ? (int)(seq_len - cs) : C;
       const int64_t done = cs + L;
@@ -1034,10 +1098,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int k = landed; k < issued; ++k)
       sm100::mbar_wait(bar_full + (k & 1), (uint32_t)((k >> 1) & 1), 200000000ull);
   } else {
-    if (nc > 0 && warp >= 6) write_out(nc - 1);
+    if (emit && nc > 0 && warp >= 6) write_out(nc - 1);
     if (s_out && involved && warp < 4) {
       const int i = tid;
-      float* dst = s_out + sbase + (int64_t)i * DV;
+      float* dst = s_out + out_base + (int64_t)i * DV;
       for (int c16 = 0; c16 < 64; c16 += 16) {
         float v[16];
         sm100::tmem_ld16(sm100::taddr(tmem, lane_q, TM_S + c16), v);
@@ -1051,6 +1115,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm100::tc_fence_before();
   __syncthreads();
   if (warp == 0) sm100::tmem_dealloc(tmem, S_TM_COLS);
+}
+
+// Entry states of the segments of a dense batch, in order: entry[s + 1] =
+// trans[s] entry[s] + s0[s] for s = 1 .. G - 2 (entry[1] is segment 0's
+// final state), the state update of a span being affine in the state that
+// enters it.  fp32 on the CUDA cores; grid (H, N, DV / 32), 256 threads:
+// thread = (key row i, 16 of the block's 32 value columns).
+constexpr int SEG_SC = 32, SEG_LDP = DK + 1;
+static_assert(DK == DV, "a transition is stored in a state's layout");
+constexpr int SEG_SMEM = (int)sizeof(float) * (DK * SEG_LDP + DK * SEG_SC);
+__global__ void __launch_bounds__(256)
+    kda_split_seg_entries_kernel(const float* trans, const float* s0, float* entry, int N,
+                                 int H, int G) {
+  extern __shared__ float sm_f[];
+  float* sP = sm_f;                 // [DK][SEG_LDP]
+  float* sS = sP + DK * SEG_LDP;    // [DK][SEG_SC]
+  const int h = blockIdx.x, n = blockIdx.y, c0 = blockIdx.z * SEG_SC;
+  const int tid = threadIdx.x, i = tid & (DK - 1), cg = (tid >> 7) * 16;
+  auto at = [&](int sg) { return (((int64_t)n * G + sg) * H + h) * (int64_t)DK * DV; };
+  for (int e = tid; e < DK * SEG_SC; e += 256)
+    sS[e] = entry[at(1) + (int64_t)(e / SEG_SC) * DV + c0 + e % SEG_SC];
+  for (int sg = 1; sg + 1 < G; ++sg) {
+    const float* P = trans + at(sg);  // [DK][DK] (DK == DV)
+    __syncthreads();
+    for (int e = tid; e < DK * DK; e += 256) sP[(e / DK) * SEG_LDP + e % DK] = P[e];
+    __syncthreads();
+    float acc[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) acc[c] = s0[at(sg) + (int64_t)i * DV + c0 + cg + c];
+    for (int k = 0; k < DK; ++k) {
+      const float pv = sP[i * SEG_LDP + k];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) acc[c] = fmaf(pv, sS[k * SEG_SC + cg + c], acc[c]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      sS[i * SEG_SC + cg + c] = acc[c];
+      entry[at(sg + 1) + (int64_t)i * DV + c0 + cg + c] = acc[c];
+    }
+  }
 }
 
 // ===========================================================================
@@ -1161,6 +1266,54 @@ PackedLayout packed_layout(int N, int T, int H, int64_t cols) {
   L.total = L.rec_at + (size_t)cols * H * REC_BYTES;
   return L;
 }
+// Segments of a dense batch on the two-kernel path.  When its state chains
+// (2 N H CTAs) leave most SMs idle and its sequences are long, each sequence
+// is cut into G segments: pass 1 runs segment 0 in full and, beside it,
+// summarises segments 1 .. G - 2 (zero-start final state and cumulative
+// transition: four state CTAs each); the entry states follow by the
+// composition rule; pass 2 reruns segments 1 .. G - 1 from them.  The
+// chain a pass runs is one segment long, so the time goes from about T to
+// 2 T / G chunk steps.  G is the most that keeps pass 1 in one wave of state
+// CTAs (one per SM), with at least 128 chunks per segment, and the records
+// of every chunk (read by both passes) within a budget.
+constexpr size_t kSegRecordBudget = (size_t)32 << 30;
+constexpr int kSegMinChunks = 128;
+// test hook: > 0 forces that many segments where the sizes allow, < 0
+// turns segments off, 0 chooses by the rule above
+std::atomic<int> g_force_segments{0};
+int split_segments(int N, int T, int H, int sms) {
+  const int64_t nchunks = ((int64_t)T + C - 1) / C;
+  const int64_t nh = (int64_t)N * H;
+  const int forced = g_force_segments.load();
+  int64_t G;
+  if (forced < 0) return 1;
+  if (forced > 0) {
+    G = forced;
+  } else {
+    if (6 * nh > sms) return 1;
+    G = 2 + (sms - 2 * nh) / (4 * nh);
+    if (G > nchunks / kSegMinChunks) G = nchunks / kSegMinChunks;
+    if (G < 3 || nh * nchunks * (int64_t)REC_BYTES > (int64_t)kSegRecordBudget) return 1;
+  }
+  // every segment holds at least one chunk: (G - 1) ceil(nchunks / G) < nchunks
+  while (G > 2 && (G - 1) * ((nchunks + G - 1) / G) >= nchunks) --G;
+  if (G < 3 || (int64_t)N * G > 65535 || 2 + 4 * (G - 2) > 65535) return 1;
+  return (int)G;
+}
+int seg_chunks(int T, int G) {
+  const int64_t nchunks = ((int64_t)T + C - 1) / C;
+  return (int)((nchunks + G - 1) / G);
+}
+// [carry][records of every chunk][entry states][zero-start states][transitions]
+size_t seg_state_bytes(int N, int H, int G) {
+  return align256((size_t)N * G * H * DK * DV * sizeof(float));
+}
+size_t split_seg_workspace_bytes(int N, int T, int H, int G) {
+  const int64_t nchunks = ((int64_t)T + C - 1) / C;
+  return carry_bytes(N, H) + (size_t)N * H * REC_BYTES * (size_t)nchunks +
+         3 * seg_state_bytes(N, H, G);
+}
+
 // chunk columns per slice of the default workspace: all of them while their
 // records fit in the record budget
 int64_t packed_default_cols(int N, int T, int H) {
@@ -1202,6 +1355,8 @@ extern "C" int kda_split_timing_read(unsigned long long* out32, int reset) {
 // the minimum holds one chunk's records per (sequence, head).
 size_t kda_split_workspace_bytes(int N, int T, int H) {
   if (N < 1 || H < 1 || T < 1) return 0;
+  const int G = split_segments(N, T, H, kda_device_sms());
+  if (G > 1) return split_seg_workspace_bytes(N, T, H, G);
   const int64_t nchunks = ((int64_t)T + C - 1) / C;
   const size_t per = (size_t)N * H * REC_BYTES;
   int64_t slice = (int64_t)(kRecordBudget / per);
@@ -1284,8 +1439,8 @@ kda_status plan_split(const kda::FwdParams& p, void* workspace, size_t workspace
 // intra, bit 1 state).
 kda_status launch_slice(const kda::FwdParams& p, const SplitPlan& pl, int c0, int cnt,
                         cudaStream_t s_intra, cudaStream_t s_state, int stages,
-                        unsigned char* rec, int grid_cap) {
-  SplitParams sp;
+                        unsigned char* rec, int grid_cap, int rec_stride = 0) {
+  SplitParams sp{};
   sp.p = p;
   sp.rec = rec;
   sp.c_begin = c0;
@@ -1298,8 +1453,9 @@ kda_status launch_slice(const kda::FwdParams& p, const SplitPlan& pl, int c0, in
   sp.s_in = c0 == 0 ? p.init_state : pl.through;
   sp.s_out = c0 + cnt == pl.nchunks ? p.final_state : pl.through;
   sp.stall_test = g_stall_test.load();
-  sp.rec_items = told_capacity((int64_t)p.N * p.H * cnt);
+  sp.rec_items = told_capacity((int64_t)p.N * p.H * (rec_stride > 0 ? rec_stride : cnt));
   sp.rows = (int64_t)p.N * p.T;
+  sp.rec_stride = rec_stride;
   if (stages & 1) {
     // persistent: two CTAs per SM walk the slice's (sequence, head, chunk) items
     const int64_t items = (int64_t)p.N * p.H * cnt;
@@ -1408,7 +1564,7 @@ kda_status packed_prepare(const kda::FwdParams& p, const SplitPlan& pl, cudaStre
 // packed_prepare), the records at the start of the workspace's record area.
 kda_status packed_slice(const kda::FwdParams& p, const SplitPlan& pl, int g0, int cnt,
                       cudaStream_t stream) {
-  SplitParams sp;
+  SplitParams sp{};
   sp.p = p;
   sp.rec = pl.rec;
   sp.c_begin = 0;
@@ -1445,6 +1601,95 @@ kda_status launch_packed(const kda::FwdParams& p, const SplitPlan& pl, cudaStrea
   return st;
 }
 
+// A dense batch in G segments (see split_segments): the records of segments
+// 0 .. G - 2, then pass 1 (segment 0 in full, the summaries of segments
+// 1 .. G - 2) and the entry states, while the last segment's records are
+// made on the SMs pass 1 leaves free; then pass 2 (segments 1 .. G - 1 in
+// full).  The kernels never wait on one another: the library's two streams
+// order them by events (as in the overlapped slice schedule; one stream
+// while the caller's stream is being captured).  The workspace holds
+// split_seg_workspace_bytes(N, T, H, G).
+kda_status run_split_segmented(const kda::FwdParams& p, const SplitPlan& pl, void* workspace,
+                               int G, cudaStream_t stream) {
+  const int L = seg_chunks(p.T, G), head = (G - 1) * L;  // chunks pass 1 reads
+  if (kda_smem_attr((const void*)kda_split_seg_entries_kernel, SEG_SMEM) != KDA_OK)
+    return KDA_ERR_CUDA;
+  float* seg = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) +
+                                        carry_bytes(p.N, p.H) +
+                                        (size_t)p.N * p.H * REC_BYTES * (size_t)pl.nchunks);
+  const size_t per = seg_state_bytes(p.N, p.H, G) / sizeof(float);
+  SplitParams sp{};
+  sp.p = p;
+  sp.rec = pl.rec;
+  sp.c_begin = 0;
+  sp.c_count = pl.nchunks;
+  sp.stall_test = g_stall_test.load();
+  sp.rec_items = told_capacity((int64_t)p.N * p.H * pl.nchunks);
+  sp.rows = (int64_t)p.N * p.T;
+  sp.seg_g = G;
+  sp.seg_len = L;
+  sp.seg_entry = seg;
+  sp.seg_s0 = seg + per;
+  sp.seg_trans = seg + 2 * per;
+  const int pass1 = (2 + 4 * (G - 2)) * p.H * p.N;  // state CTAs of pass 1
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  const bool side = cudaStreamIsCapturing(stream, &cap) == cudaSuccess &&
+                    cap == cudaStreamCaptureStatusNone && pass1 < pl.sms;
+  std::unique_lock<std::mutex> lock(g_ov_mu, std::defer_lock);
+  OverlapRes* r = nullptr;
+  if (side) {
+    lock.lock();
+    if (overlap_res(&r) != KDA_OK) return KDA_ERR_CUDA;
+  }
+  kda_status st = KDA_OK;
+  auto cu = [&](cudaError_t e) {
+    if (e != cudaSuccess && st == KDA_OK) st = KDA_ERR_CUDA;
+  };
+  // records of segments 0 .. G - 2 on the caller's stream
+  st = launch_slice(p, pl, 0, head, stream, stream, 1, pl.rec, 2 * pl.sms, pl.nchunks);
+  cudaStream_t s_state = stream, s_intra = stream;
+  if (side && st == KDA_OK) {
+    s_state = r->s_state;
+    s_intra = r->s_intra;
+    cu(cudaEventRecord(r->ev_start, stream));
+    cu(cudaStreamWaitEvent(s_state, r->ev_start, 0));
+    cu(cudaStreamWaitEvent(s_intra, r->ev_start, 0));
+  }
+  if (st == KDA_OK) {
+    sp.seg_pass = 1;
+    kda_tc_state_kernel<<<dim3(2 + 4 * (G - 2), p.H, p.N), kThreads, S_SMEM, s_state>>>(pl.mv,
+                                                                                       sp);
+    cu(cudaGetLastError());
+  }
+  if (st == KDA_OK) {
+    kda_split_seg_entries_kernel<<<dim3(p.H, p.N, DV / SEG_SC), 256, SEG_SMEM, s_state>>>(
+        sp.seg_trans, sp.seg_s0, sp.seg_entry, p.N, p.H, G);
+    cu(cudaGetLastError());
+  }
+  // the last segment's records beside pass 1 (its CTAs take whole SMs)
+  if (st == KDA_OK) {
+    const int cap_beside = side ? 2 * (pl.sms - pass1) : 2 * pl.sms;
+    st = launch_slice(p, pl, head, pl.nchunks - head, s_intra, s_intra, 1, pl.rec, cap_beside,
+                      pl.nchunks);
+  }
+  if (side) {
+    cu(cudaEventRecord(r->ev_intra[0], s_intra));
+    cu(cudaStreamWaitEvent(s_state, r->ev_intra[0], 0));
+  }
+  if (st == KDA_OK) {
+    sp.seg_pass = 2;
+    kda_tc_state_kernel<<<dim3(2 * (G - 1), p.H, p.N), kThreads, S_SMEM, s_state>>>(pl.mv, sp);
+    cu(cudaGetLastError());
+  }
+  if (side) {
+    // the caller's stream continues once pass 2 is done (which follows
+    // every other launch of the call)
+    cu(cudaEventRecord(r->ev_state[0], s_state));
+    cu(cudaStreamWaitEvent(stream, r->ev_state[0], 0));
+  }
+  return st;
+}
+
 kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_bytes,
                      cudaStream_t stream, int stages, bool one_slice) {
   SplitPlan pl;
@@ -1453,6 +1698,12 @@ kda_status run_split(const kda::FwdParams& p, void* workspace, size_t workspace_
   if (pl.packed) return stages == 3 ? launch_packed(p, pl, stream) : KDA_ERR_UNSUPPORTED;
   const int slice = pl.fit < (size_t)pl.nchunks ? (int)pl.fit : pl.nchunks;
   if (one_slice && slice < pl.nchunks) return KDA_ERR_WORKSPACE;
+  // few long chains and room for every record: segments
+  if (stages == 3 && !one_slice && !p.ckpt) {
+    const int G = split_segments(p.N, p.T, p.H, pl.sms);
+    if (G > 1 && workspace_bytes >= split_seg_workspace_bytes(p.N, p.T, p.H, G))
+      return run_split_segmented(p, pl, workspace, G, stream);
+  }
   // more than one slice and state chains on at most half of the SMs: the
   // overlapped schedule (not while the caller's stream is being captured)
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -1545,6 +1796,11 @@ extern "C" kda_status kda_split_stage(int stage, const uint16_t* q, const uint16
 // Test hook: the next calls of the two-kernel path make their first wait in
 // the intra kernel (flags bit 0) and / or the state kernel (bit 1) run out
 // (see SplitParams::stall_test); 0 restores normal calls.
+extern "C" kda_status kda_debug_split_segments(int segments) {
+  g_force_segments.store(segments);
+  return KDA_OK;
+}
+
 extern "C" kda_status kda_debug_stall_test(int flags) {
   if (flags < 0 || flags > 3) return KDA_ERR_INVALID_ARG;
   g_stall_test.store(flags);

@@ -62,6 +62,7 @@ _SIGS = {
                                                         _vp, _vp]),
     "kda_debug_intra": (_i, [_vp] * 5 + [_i] * 5 + [_vp, _i, _i] + [_vp] * 6 + [_vp]),
     "kda_debug_stall_test": (_i, [_i]),
+    "kda_debug_split_segments": (_i, [_i]),
     "kda_segment_summary": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _vp]),
     "kda_summary_floats": (ctypes.c_size_t, [_i] * 4),
     "kda_state_compose": (_i, [_vp, _i, _vp, _vp] + [_i] * 4 + [_vp]),
@@ -267,6 +268,13 @@ def kda_debug_stall_test(flags: int) -> int:
     """Test hook: make the two-kernel path's first waits run out (bit 0 intra
     kernel, bit 1 state kernel); 0 restores normal calls."""
     return load().kda_debug_stall_test(int(flags))
+
+
+def kda_debug_split_segments(segments: int) -> int:
+    """Test hook: force that many segments per sequence on the two-kernel
+    path for dense batches (> 0), turn segments off (< 0) or restore the
+    automatic choice (0)."""
+    return load().kda_debug_split_segments(int(segments))
 
 
 def kda_debug_record_capacity(items: int) -> int:

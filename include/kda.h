@@ -130,6 +130,15 @@ kda_status kda_chunk_fwd_f32(const float* q, const float* k, const float* v,
  *               runs the sequence in more, shorter slices; below that
  *               KDA_ERR_WORKSPACE.  A packed batch needs the full size
  *               (every chunk column, ceil(T / 64) + N at most, at once).
+ *               For a dense batch of few long sequences (6 N H state
+ *               CTAs at most one per SM, 384 chunks or more per sequence)
+ *               kda_workspace_bytes asks for the records of every chunk
+ *               (N * H * ceil(T / 64) * 66048 bytes, at most 32 GiB) plus
+ *               three [N][G][H][dk][dv] fp32 state buffers, and the call
+ *               cuts each sequence into G segments run side by side
+ *               (segment summaries, their composition into entry states,
+ *               then the reruns); a smaller workspace runs the plain
+ *               sliced form.
  *   dev_status  NULL or one device int32; set to KDA_OK at the start of the
  *               work and to a device-detected error if one occurs.
  */
@@ -358,6 +367,16 @@ kda_status kda_split_stage(int stage, const uint16_t* q, const uint16_t* k, cons
  * the pages: it exists to test the library's own failure path.
  */
 kda_status kda_debug_stall_test(int flags);
+
+/*
+ * Test hook for the segmented two-kernel form (see kda_chunk_fwd_ex's
+ * workspace): segments > 0 makes dense batches on that path use that many
+ * segments per sequence wherever each segment still holds a chunk (three
+ * at least; kda_workspace_bytes follows), segments < 0 turns the form off,
+ * 0 restores the automatic choice.  Process-wide; not thread-safe against
+ * concurrent calls.  Always KDA_OK.
+ */
+kda_status kda_debug_split_segments(int segments);
 
 /*
  * Debug builds (compiled with -DKDA_DEBUG; kda_build_info() says so): the

@@ -109,6 +109,32 @@ def test_staging_bytes_of_the_pipelined_host_call(lib):
 
 
 
+def test_workspace_of_the_segmented_two_kernel_form(lib):
+    # with segments forced, a dense batch on the two-kernel path asks for the
+    # records of every chunk and three [N][G][H][128][128] fp32 state buffers
+    # (entry states, zero-start states, transitions) after the carried state
+    def r256(x):
+        return (x + 255) // 256 * 256
+    N, T, H = 2, 1500, 3
+    nchunks = (T + 63) // 64
+    carry = r256(N * H * 128 * 128 * 4)
+    try:
+        assert kda.kda_debug_split_segments(3) == 0
+        n3 = kda.kda_workspace_bytes(N, T, H, 128, 128, kda.KDA_BF16, 0, kda.KDA_ALGO_SPLIT, 0)
+        assert n3 == carry + N * H * nchunks * 66048 + 3 * r256(N * 3 * H * 128 * 128 * 4)
+        # five asked for, four possible (every segment holds a chunk: 11 chunks)
+        kda.kda_debug_split_segments(5)
+        n4 = kda.kda_workspace_bytes(1, 645, 2, 128, 128, kda.KDA_BF16, 0,
+                                     kda.KDA_ALGO_SPLIT, 0)
+        assert n4 == r256(2 * 128 * 128 * 4) + 2 * 11 * 66048 + 3 * r256(4 * 2 * 128 * 128 * 4)
+        # off: the plain sliced form
+        kda.kda_debug_split_segments(-1)
+        n0 = kda.kda_workspace_bytes(N, T, H, 128, 128, kda.KDA_BF16, 0, kda.KDA_ALGO_SPLIT, 0)
+        assert n0 == carry + N * H * nchunks * 66048
+    finally:
+        kda.kda_debug_split_segments(0)
+
+
 def test_staging_bytes_of_the_pipelined_packed_host_call(lib):
     # a packed bf16 batch at dk = dv = 128 runs in up to eight pieces of chunk
     # columns (of the bound ceil(T / 64) + N): the staging holds the inputs,
