@@ -353,15 +353,29 @@ def run_ours(args):
     split = path == kda.KDA_ALGO_SPLIT
     launches_per_step = 1
     split_ms = {}
+    segments = 1
     if split:
         rec = 66048  # bytes of one chunk record
         sws = ws_bytes
         carry = (N * H * dk * dv * 4 + 255) // 256 * 256
         nchunks = (T + 63) // 64
-        slice_chunks = (ws_bytes - carry) // (N * H * rec)
-        launches_per_step = 2 * ((nchunks + slice_chunks - 1) // slice_chunks)
+        if w.varlen:
+            # [carry][chunk offsets][chunk table][records of a slice of columns];
+            # the chunk table costs two launches, each slice two more
+            g_max = nchunks + N
+            rec_at = carry + (((N + 1) * 4 + 255) // 256 + (g_max * 8 + 255) // 256) * 256
+            cols = (ws_bytes - rec_at) // (H * rec)
+            launches_per_step = 2 + 2 * ((g_max + cols - 1) // cols)
+            one_slice = False
+        else:
+            segments = kda.kda_split_segment_count(N, T, H, ws_bytes)
+            slice_chunks = (ws_bytes - carry) // (N * H * rec)
+            # the segmented form: the first segments' records, pass 1, the
+            # entry states, the last segment's records, pass 2
+            launches_per_step = 5 if segments > 1 else \
+                2 * ((nchunks + slice_chunks - 1) // slice_chunks)
+            one_slice = segments == 1 and slice_chunks >= nchunks
         swork = work
-        one_slice = slice_chunks >= nchunks
 
         def stage(sg):
             return kda.kda_split_stage(sg, d["q"], d["k"], d["v"], d["g"], d["beta"],
@@ -423,11 +437,17 @@ def run_ours(args):
         # the path is two kernels; the roofline is taken over the pair (one
         # forward), each kernel's own time and traffic listed beside it
         kname = "kda_tc_intra_kernel + kda_tc_state_kernel"
-        tr = [ncu_traffic(k, w.name) for k in ("kda_tc_intra_kernel", "kda_tc_state_kernel")]
-        traffic = sum(tr) if all(t is not None for t in tr) else None
-        tot = sum(split_ms.values()) if split_ms else None
-        kernels = {k: {"ms": v, "share": v / tot, "dram_bytes": ncu_traffic(k, w.name)}
-                   for k, v in split_ms.items()} if split_ms else None
+        if segments > 1:
+            # the segmented form (two state passes and the entry states):
+            # the per-kernel times taken alone would describe the plain form
+            kname += " (%d segments per sequence)" % segments
+        else:
+            tr = [ncu_traffic(k, w.name) for k in ("kda_tc_intra_kernel",
+                                                   "kda_tc_state_kernel")]
+            traffic = sum(tr) if all(t is not None for t in tr) else None
+            tot = sum(split_ms.values()) if split_ms else None
+            kernels = {k: {"ms": v, "share": v / tot, "dram_bytes": ncu_traffic(k, w.name)}
+                       for k, v in split_ms.items()} if split_ms else None
     else:
         traffic = ncu_traffic(kname, w.name)
     kernel_ms = float(np.mean(launch_ms))

@@ -1245,8 +1245,13 @@ int64_t told_capacity(int64_t real) {
   return o > 0 && o < real ? o : real;
 }
 
-// default bytes of records held at once (the slice length follows from it)
+// default bytes of records held at once (the slice length follows from it):
+// a dense batch's slices, and a packed batch's (whose sequences end at
+// different chunk columns, so each slice waits for its longest chain: one
+// slice is best, 12.1 against 13.4 ms for a 1M-token batch of 28 sequences
+// in five)
 constexpr size_t kRecordBudget = (size_t)4 << 30;
+constexpr size_t kPackedRecordBudget = (size_t)32 << 30;
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t carry_bytes(int N, int H) { return align256((size_t)N * H * DK * DV * sizeof(float)); }
@@ -1318,7 +1323,7 @@ size_t split_seg_workspace_bytes(int N, int T, int H, int G) {
 // records fit in the record budget
 int64_t packed_default_cols(int N, int T, int H) {
   const int64_t g = packed_g_max(N, T);
-  int64_t fit = (int64_t)(kRecordBudget / ((size_t)H * REC_BYTES));
+  int64_t fit = (int64_t)(kPackedRecordBudget / ((size_t)H * REC_BYTES));
   if (fit < 1) fit = 1;
   return g < fit ? g : fit;
 }
@@ -1796,6 +1801,14 @@ extern "C" kda_status kda_split_stage(int stage, const uint16_t* q, const uint16
 // Test hook: the next calls of the two-kernel path make their first wait in
 // the intra kernel (flags bit 0) and / or the state kernel (bit 1) run out
 // (see SplitParams::stall_test); 0 restores normal calls.
+// Segments per sequence a dense bf16 call at dk = dv = 128 on the
+// two-kernel path takes with this workspace (1: the plain form).
+extern "C" int kda_split_segment_count(int N, int T, int H, size_t workspace_bytes) {
+  if (N < 1 || H < 1 || T < 1) return 1;
+  const int G = split_segments(N, T, H, kda_device_sms());
+  return G > 1 && workspace_bytes >= split_seg_workspace_bytes(N, T, H, G) ? G : 1;
+}
+
 extern "C" kda_status kda_debug_split_segments(int segments) {
   g_force_segments.store(segments);
   return KDA_OK;

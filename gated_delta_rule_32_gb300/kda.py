@@ -63,6 +63,7 @@ _SIGS = {
     "kda_debug_intra": (_i, [_vp] * 5 + [_i] * 5 + [_vp, _i, _i] + [_vp] * 6 + [_vp]),
     "kda_debug_stall_test": (_i, [_i]),
     "kda_debug_split_segments": (_i, [_i]),
+    "kda_split_segment_count": (_i, [_i, _i, _i, ctypes.c_size_t]),
     "kda_segment_summary": (_i, [_vp] * 6 + [_i] * 5 + [_vp, _vp]),
     "kda_summary_floats": (ctypes.c_size_t, [_i] * 4),
     "kda_state_compose": (_i, [_vp, _i, _vp, _vp] + [_i] * 4 + [_vp]),
@@ -275,6 +276,12 @@ def kda_debug_split_segments(segments: int) -> int:
     path for dense batches (> 0), turn segments off (< 0) or restore the
     automatic choice (0)."""
     return load().kda_debug_split_segments(int(segments))
+
+
+def kda_split_segment_count(N: int, T: int, H: int, workspace_bytes: int) -> int:
+    """Segments per sequence the two-kernel path takes for a dense batch with
+    this workspace (1: the plain form)."""
+    return load().kda_split_segment_count(int(N), int(T), int(H), int(workspace_bytes))
 
 
 def kda_debug_record_capacity(items: int) -> int:

@@ -81,15 +81,13 @@ typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
 /* Implementation choice for kda_chunk_fwd_ex (the result is the same
  * function of the inputs up to rounding). */
 typedef enum {
-  KDA_ALGO_AUTO = 0,  /* tensor-core path where built (two-kernel form; the fused
-                       * kernel for a packed batch whose chunk records would pass
-                       * 4 GiB), else CUDA-core */
+  KDA_ALGO_AUTO = 0,  /* tensor-core path where built (the two-kernel form at
+                       * dk = dv = 128), else CUDA-core */
   KDA_ALGO_SIMT = 1,  /* fp32 CUDA-core chunked path (16-token chunks) */
   KDA_ALGO_TC = 2,    /* tcgen05/TMEM/TMA fused path (bf16, dk = dv = 128) */
   KDA_ALGO_SPLIT = 3  /* tensor-core path in two kernels (bf16, dk = dv = 128): every
                        * chunk's state-independent part at once, then the serial
-                       * state pass; needs a workspace (packed batches: all
-                       * records at once) */
+                       * state pass; needs a workspace */
 } kda_algo;
 
 /* Human-readable name of a status code (static storage). */
@@ -377,6 +375,12 @@ kda_status kda_debug_stall_test(int flags);
  * concurrent calls.  Always KDA_OK.
  */
 kda_status kda_debug_split_segments(int segments);
+
+/* Segments per sequence that kda_chunk_fwd_ex on the two-kernel path
+ * (dense bf16 batch, dk = dv = 128, on the current device) cuts each
+ * sequence into with a workspace of workspace_bytes: 1 for the plain form.
+ * Host-only; a query for schedulers and benchmarks. */
+int kda_split_segment_count(int N, int T, int H, size_t workspace_bytes);
 
 /*
  * Debug builds (compiled with -DKDA_DEBUG; kda_build_info() says so): the

@@ -122,6 +122,9 @@ def test_workspace_of_the_segmented_two_kernel_form(lib):
         assert kda.kda_debug_split_segments(3) == 0
         n3 = kda.kda_workspace_bytes(N, T, H, 128, 128, kda.KDA_BF16, 0, kda.KDA_ALGO_SPLIT, 0)
         assert n3 == carry + N * H * nchunks * 66048 + 3 * r256(N * 3 * H * 128 * 128 * 4)
+        # the form a call takes follows the workspace it is given
+        assert kda.kda_split_segment_count(N, T, H, n3) == 3
+        assert kda.kda_split_segment_count(N, T, H, n3 - 1) == 1
         # five asked for, four possible (every segment holds a chunk: 11 chunks)
         kda.kda_debug_split_segments(5)
         n4 = kda.kda_workspace_bytes(1, 645, 2, 128, 128, kda.KDA_BF16, 0,
@@ -191,23 +194,27 @@ def test_packed_workspace_sizes(lib):
     # [carry][chunk offsets][chunk table][records of a slice of chunk columns]
     def r256(x):
         return (x + 255) // 256 * 256
+    # (by default the records of every column while they fit in 32 GiB)
     N, T, H = 3, 1 << 20, 16
     g_max = T // 64 + N
     rec_at = r256(N * H * 128 * 128 * 4) + r256((N + 1) * 4) + r256(g_max * 8)
-    cols = (4 << 30) // (H * 66048)
+    assert kda.kda_workspace_bytes(N, T, H, 128, 128, packed=1) == rec_at + g_max * H * 66048
+    N, T, H = 3, 1 << 21, 16
+    g_max = T // 64 + N
+    rec_at = r256(N * H * 128 * 128 * 4) + r256((N + 1) * 4) + r256(g_max * 8)
+    cols = (32 << 30) // (H * 66048)
     assert cols < g_max
     assert kda.kda_workspace_bytes(N, T, H, 128, 128, packed=1) == rec_at + cols * H * 66048
 
 
 def test_resolve_path(lib):
-    # the automatic path of a bf16 batch is the two-kernel form (a packed one
-    # while all its chunk records fit in 4 GiB, else the fused kernel), fp32
-    # inputs take the CUDA-core path
+    # the automatic path of a bf16 batch at d = 128 is the two-kernel form,
+    # fp32 inputs and other head sizes take the CUDA-core path
     rp = kda.kda_resolve_path
     assert rp(2, 32768, 32) == kda.KDA_ALGO_SPLIT
     assert rp(2, 32768, 32, packed=True) == kda.KDA_ALGO_SPLIT
     # a packed batch too long to hold every chunk record at once runs in
-    # slices of chunk columns, its default workspace capped at 4 GiB of records
+    # slices of chunk columns, its default workspace capped at 32 GiB of records
     assert rp(1, 1 << 20, 16, packed=True) == kda.KDA_ALGO_SPLIT
     assert rp(2, 32768, 32, algo=kda.KDA_ALGO_TC) == kda.KDA_ALGO_TC
     assert rp(2, 100, 4, dtype=kda.KDA_F32) == kda.KDA_ALGO_SIMT

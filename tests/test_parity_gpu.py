@@ -251,12 +251,34 @@ def test_full_ctx1m_sampled():
 
 
 def test_full_varlen_ctx1m_sampled():
-    # 1M tokens packed in ~32 sequences: more chunk records than the default
-    # workspace holds, so the two-kernel path runs in slices of chunk columns
-    # and sequences carry their state across slices
+    # 1M tokens packed in 28 sequences: the default workspace holds every
+    # chunk column's records (one slice); with 4 GiB of records the same
+    # call runs in slices of chunk columns, sequences carrying their state
+    # across them, and must give the same bits
     w = WORKLOADS["varlen_ctx1m"]
-    assert kda.kda_resolve_path(w.n_seqs(), w.T, w.H, packed=True) == kda.KDA_ALGO_SPLIT
-    g_max = w.T // 64 + w.n_seqs()
-    assert kda.kda_workspace_bytes(w.n_seqs(), w.T, w.H, 128, 128, packed=1) < \
-        g_max * w.H * 66048
+    N, T, H = w.n_seqs(), w.T, w.H
+    assert kda.kda_resolve_path(N, T, H, packed=True) == kda.KDA_ALGO_SPLIT
+    g_max = T // 64 + N
+    full = kda.kda_workspace_bytes(N, T, H, 128, 128, packed=1)
+    assert full >= g_max * H * 66048
     _sampled_check("varlen_ctx1m", [(0, 9)])
+    x = make_inputs(w)
+    d = to_dev(x)
+
+    def run(nb):
+        ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(d["v"])
+        fs = torch.empty(N, H, 128, 128, device="cuda")
+        rc = kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                                  out, fs, N, T, H, 128, 128, d["cu_seqlens"], kda.KDA_BF16, 0,
+                                  1.0, kda.KDA_ALGO_SPLIT, ws, nb, None,
+                                  torch.cuda.current_stream())
+        assert rc == 0, kda.status_string(rc)
+        del ws
+        return out, fs
+    o1, s1 = run(full)
+    cols = (4 << 30) // (H * 66048)
+    assert cols < g_max
+    o2, s2 = run(full - (g_max - cols) * H * 66048)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
