@@ -132,3 +132,27 @@ def test_segment_state_stall_reports_timeout():
     o, s, _ = run(x, 3)
     np.testing.assert_array_equal(o, clean_o)
     np.testing.assert_array_equal(s, clean_s)
+
+
+def test_segments_update_the_state_in_place():
+    """init_state and final_state may be one buffer: segment 0 reads it in
+    pass 1, the last segment writes it at the end of pass 2."""
+    w = small_workload("segsplit5", B=2, T=1100, H=2, dk=128, dv=128, s0_std=0.03, seed=65)
+    x = make_inputs(w)
+    o_ref, s_ref = run(x, 3)[:2]
+    kda.kda_debug_split_segments(3)
+    try:
+        d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
+        nb = kda.kda_workspace_bytes(2, 1100, 2, 128, 128, kda.KDA_BF16, 0, SPLIT, 0)
+        ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        out = torch.empty_like(d["v"])
+        st = d["init_state"].clone()
+        rc = kda.kda_chunk_fwd_ex(d["q"], d["k"], d["v"], d["g"], d["beta"], st, out, st, 2,
+                                  1100, 2, 128, 128, None, kda.KDA_BF16, 0, 1.0, SPLIT, ws, nb,
+                                  None, torch.cuda.current_stream())
+        assert rc == 0, kda.status_string(rc)
+        torch.cuda.synchronize()
+    finally:
+        kda.kda_debug_split_segments(0)
+    np.testing.assert_array_equal(out.float().cpu().numpy(), o_ref)
+    np.testing.assert_array_equal(st.cpu().numpy(), s_ref)
