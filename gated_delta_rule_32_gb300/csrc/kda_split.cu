@@ -1,4 +1,4 @@
-// kda_split.cu -- the two-kernel tensor-core forward for dense batches.
+// kda_split.cu -- the two-kernel tensor-core forward (dense and packed batches).
 //
 // Everything of a chunk that does not depend on the state entering it (the
 // gate, the Gram matrices, T = (I + beta A_kk)^{-1}, W = T (beta K gamma),
@@ -25,7 +25,13 @@
 //
 // A long sequence runs in slices of chunks (intra kernel over the slice,
 // then the state kernel over it), so the record buffer stays bounded; the
-// state crosses slice boundaries through global memory.
+// state crosses slice boundaries through global memory.  Packed batches
+// (cu_seqlens) run in slices of chunk columns.  A dense batch of few long
+// sequences is cut into segments whose chains run side by side, joined by
+// the affine composition of each segment's zero-start state and cumulative
+// transition (orkas.ai, "Kimi K3 architecture", "The cost is paid in the
+// serving stack": the context-parallel decomposition, here across the SMs
+// of one GPU).
 #include <cudaTypedefs.h>
 #include <string.h>
 
