@@ -360,12 +360,14 @@ def run_ours(args):
         carry = (N * H * dk * dv * 4 + 255) // 256 * 256
         nchunks = (T + 63) // 64
         if w.varlen:
-            # [carry][chunk offsets][chunk table][records of a slice of columns];
-            # the chunk table costs two launches, each slice two more
+            # [carry][chunk offsets][sequence order][chunk table][records of a
+            # slice of columns]; the chunk table and the order cost three
+            # launches, each slice two more
             g_max = nchunks + N
-            rec_at = carry + (((N + 1) * 4 + 255) // 256 + (g_max * 8 + 255) // 256) * 256
+            rec_at = carry + (((N + 1) * 4 + 255) // 256 + (N * 4 + 255) // 256 +
+                              (g_max * 8 + 255) // 256) * 256
             cols = (ws_bytes - rec_at) // (H * rec)
-            launches_per_step = 2 + 2 * ((g_max + cols - 1) // cols)
+            launches_per_step = 3 + 2 * ((g_max + cols - 1) // cols)
             one_slice = False
         else:
             segments = kda.kda_split_segment_count(N, T, H, ws_bytes)

@@ -88,6 +88,8 @@ struct SplitParams {
   // slice is the columns [g_begin, g_begin + g_count)
   const int2* chunk_tab;  // [g_max], null for dense batches
   const int* chunk_off;   // [N + 1]
+  // the sequence each state CTA z runs (longest first), [N]; null: z itself
+  const int* seq_order;
   int g_max;              // chunk columns: ceil(T / 64) + N bounds the true count
   int g_begin, g_count;
   // extents the debug build checks accesses against: chunk records the
@@ -745,7 +747,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const kda::FwdParams& p = sp.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg_g = sp.seg_g > 1 ? sp.seg_g : 1;
-  const int half = blockIdx.x & 1, h = blockIdx.y, n = blockIdx.z, H = p.H;
+  const int half = blockIdx.x & 1, h = blockIdx.y, H = p.H;
+  const int n = sp.seq_order ? sp.seq_order[blockIdx.z] : (int)blockIdx.z;
   // segments: pass 1 grid x = [segment 0: 2 halves][segments 1 .. G - 2:
   // (state run, transition run) x 2 halves], pass 2 grid x = [segments
   // 1 .. G - 1: 2 halves].  A transition run starts from the identity, with
@@ -1167,6 +1170,31 @@ __global__ void __launch_bounds__(256)
 // ===========================================================================
 // packed batches: the chunk columns of the sequences
 // ===========================================================================
+// The order in which the state CTAs take the sequences: longest first.  A
+// sequence's chain is the longest single piece of work of the state pass,
+// and the CTAs start in grid order, so a long sequence placed last would run
+// on alone at the end.  order[rank] = n with rank = the number of sequences
+// with more chunks, or as many and a lower index (a permutation, also for
+// the all-zero offsets of a malformed batch); beyond kOrderMax sequences
+// the count of comparisons is not worth it and the order is the identity.
+constexpr int kOrderMax = 8192;
+__global__ void __launch_bounds__(256)
+    kda_split_order_kernel(const int* off, int N, int* order) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  if (N > kOrderMax) {
+    order[n] = n;
+    return;
+  }
+  const int c = off[n + 1] - off[n];
+  int rank = 0;
+  for (int m = 0; m < N; ++m) {
+    const int cm = off[m + 1] - off[m];
+    rank += (cm > c || (cm == c && m < n)) ? 1 : 0;
+  }
+  order[rank] = n;
+}
+
 // One CTA: off[n] = chunks of the sequences before n (an exclusive scan of
 // ceil(len / 64)), off[N] = their total.  Malformed offsets (cu[0] != 0,
 // cu[N] != T, a decreasing pair) are reported through the status word and
@@ -1262,17 +1290,18 @@ constexpr size_t kPackedRecordBudget = (size_t)32 << 30;
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t carry_bytes(int N, int H) { return align256((size_t)N * H * DK * DV * sizeof(float)); }
 
-// packed batches: [carry][chunk_off: N + 1 ints][chunk_tab: g_max
-// entries][records: H x the chunk columns of one slice]
+// packed batches: [carry][chunk_off: N + 1 ints][seq_order: N ints]
+// [chunk_tab: g_max entries][records: H x the chunk columns of one slice]
 int packed_g_max(int N, int T) { return (int)(((int64_t)T + C - 1) / C + N); }
 struct PackedLayout {
-  size_t off_at, tab_at, rec_at, total;
+  size_t off_at, ord_at, tab_at, rec_at, total;
 };
 PackedLayout packed_layout(int N, int T, int H, int64_t cols) {
   PackedLayout L;
   const size_t g = (size_t)packed_g_max(N, T);
   L.off_at = carry_bytes(N, H);
-  L.tab_at = L.off_at + align256((size_t)(N + 1) * sizeof(int));
+  L.ord_at = L.off_at + align256((size_t)(N + 1) * sizeof(int));
+  L.tab_at = L.ord_at + align256((size_t)N * sizeof(int));
   L.rec_at = L.tab_at + align256(g * sizeof(int2));
   L.total = L.rec_at + (size_t)cols * H * REC_BYTES;
   return L;
@@ -1396,6 +1425,7 @@ struct SplitPlan {
   bool packed = false;
   int g_max = 0;
   int* chunk_off = nullptr;
+  int* seq_order = nullptr;
   int2* chunk_tab = nullptr;
 };
 
@@ -1414,6 +1444,7 @@ kda_status plan_split(const kda::FwdParams& p, void* workspace, size_t workspace
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     pl.g_max = packed_g_max(p.N, p.T);
     pl.chunk_off = reinterpret_cast<int*>(ws + L.off_at);
+    pl.seq_order = reinterpret_cast<int*>(ws + L.ord_at);
     pl.chunk_tab = reinterpret_cast<int2*>(ws + L.tab_at);
     pl.per = (size_t)p.H * REC_BYTES;  // records of one chunk column
     pl.fit = (workspace_bytes - L.rec_at) / pl.per;
@@ -1564,6 +1595,8 @@ kda_status run_overlapped(const kda::FwdParams& p, const SplitPlan& pl, int slic
 kda_status packed_prepare(const kda::FwdParams& p, const SplitPlan& pl, cudaStream_t stream) {
   kda_split_offsets_kernel<<<1, 1024, 0, stream>>>(p.cu_seqlens, p.N, p.T, pl.chunk_off,
                                                    p.dev_status);
+  kda_split_order_kernel<<<(p.N + 255) / 256, 256, 0, stream>>>(pl.chunk_off, p.N,
+                                                                pl.seq_order);
   const int tb_need = (pl.g_max + 255) / 256;
   const int tb = tb_need < 8 * pl.sms ? tb_need : 8 * pl.sms;
   kda_split_table_kernel<<<tb, 256, 0, stream>>>(p.cu_seqlens, pl.chunk_off, p.N, pl.g_max,
@@ -1586,6 +1619,7 @@ kda_status packed_slice(const kda::FwdParams& p, const SplitPlan& pl, int g0, in
   sp.s_out = pl.through;
   sp.chunk_tab = pl.chunk_tab;
   sp.chunk_off = pl.chunk_off;
+  sp.seq_order = pl.seq_order;
   sp.g_max = pl.g_max;
   sp.g_begin = g0;
   sp.g_count = cnt;

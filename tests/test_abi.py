@@ -150,7 +150,7 @@ def test_staging_bytes_of_the_pipelined_packed_host_call(lib):
     fixed = 5 * r256(qk) + r256(T * H * 2) + 2 * r256(state) + r256((N + 1) * 4) + 256
     g_max = (T + 63) // 64 + N
     per = (g_max + 7) // 8
-    piece = r256(state) + r256((N + 1) * 4) + r256(g_max * 8) + per * H * 66048
+    piece = r256(state) + r256((N + 1) * 4) + r256(N * 4) + r256(g_max * 8) + per * H * 66048
     n = kda.kda_host_staging_bytes(N, T, H, 128, 128, kda.KDA_BF16, 1, 1, 1)
     assert n == fixed + r256(piece)
 
@@ -168,7 +168,7 @@ def test_split_path_host_checks(lib):
     # workspace sizing of the two-kernel path: carried state + one slice of
     # 66048-byte chunk records per (sequence, head); a packed batch keeps
     # every chunk column (ceil(T / 64) + N of them at most) at once, after
-    # its chunk offsets and chunk table
+    # its chunk offsets, sequence order and chunk table
     carry = 2 * 32 * 128 * 128 * 4
     nb = kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=kda.KDA_ALGO_SPLIT)
     assert nb == carry + 2 * 32 * 512 * 66048
@@ -176,7 +176,7 @@ def test_split_path_host_checks(lib):
         2 * 128 * 128 * 4 + 2 * 2 * 66048
     g_max = 32768 // 64 + 2
     assert kda.kda_workspace_bytes(2, 32768, 32, 128, 128, algo=kda.KDA_ALGO_SPLIT,
-                                   packed=1) == carry + 256 + 4352 + 32 * g_max * 66048
+                                   packed=1) == carry + 256 + 256 + 4352 + 32 * g_max * 66048
     assert g_max * 8 <= 4352
     assert kda.kda_resolve_algo(kda.KDA_BF16, 128, 128, 0, kda.KDA_ALGO_SPLIT) == \
         kda.KDA_ALGO_SPLIT
@@ -191,17 +191,18 @@ def test_split_path_host_checks(lib):
 
 
 def test_packed_workspace_sizes(lib):
-    # [carry][chunk offsets][chunk table][records of a slice of chunk columns]
+    # [carry][chunk offsets][sequence order][chunk table][records of a slice of
+    # chunk columns]
     def r256(x):
         return (x + 255) // 256 * 256
     # (by default the records of every column while they fit in 32 GiB)
     N, T, H = 3, 1 << 20, 16
     g_max = T // 64 + N
-    rec_at = r256(N * H * 128 * 128 * 4) + r256((N + 1) * 4) + r256(g_max * 8)
+    rec_at = r256(N * H * 128 * 128 * 4) + r256((N + 1) * 4) + r256(N * 4) + r256(g_max * 8)
     assert kda.kda_workspace_bytes(N, T, H, 128, 128, packed=1) == rec_at + g_max * H * 66048
     N, T, H = 3, 1 << 21, 16
     g_max = T // 64 + N
-    rec_at = r256(N * H * 128 * 128 * 4) + r256((N + 1) * 4) + r256(g_max * 8)
+    rec_at = r256(N * H * 128 * 128 * 4) + r256((N + 1) * 4) + r256(N * 4) + r256(g_max * 8)
     cols = (32 << 30) // (H * 66048)
     assert cols < g_max
     assert kda.kda_workspace_bytes(N, T, H, 128, 128, packed=1) == rec_at + cols * H * 66048

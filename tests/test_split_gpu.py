@@ -238,11 +238,12 @@ def run_packed(x, algo=SPLIT, status=None, workspace=True, ws_bytes=None, final=
 
 
 def packed_min_ws(N, T, H):
-    # [carry][chunk offsets][chunk table][records of one chunk column]
+    # [carry][chunk offsets][sequence order][chunk table][records of one chunk column]
     def r256(v):
         return (v + 255) // 256 * 256
     g_max = (T + 63) // 64 + N
-    return (r256(N * H * 128 * 128 * 4) + r256((N + 1) * 4) + r256(g_max * 8) + H * REC)
+    return (r256(N * H * 128 * 128 * 4) + r256((N + 1) * 4) + r256(N * 4) + r256(g_max * 8) +
+            H * REC)
 
 
 @pytest.mark.parametrize("extra_cols", [0, 2, 5])
