@@ -26,8 +26,12 @@ def main():
     res = {"info": kda.kda_build_info()}
     cases = {"dense": small_workload("dbg", B=2, T=300, H=2, seed=71, s0_std=0.05),
              "packed": small_workload("dbgp", B=1, T=461, H=2, seed=72, varlen=True,
-                                      lengths=(100, 1, 64, 296))}
+                                      lengths=(100, 1, 64, 296)),
+             # the segmented form (three segments forced): records of every
+             # chunk, two state passes
+             "segmented": small_workload("dbgs", B=1, T=1000, H=2, seed=73, s0_std=0.05)}
     for name, w in cases.items():
+        kda.kda_debug_split_segments(3 if name == "segmented" else 0)
         x = make_inputs(w)
         d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in x.items()}
         N, T, H = x["B"], x["T"], x["H"]
@@ -57,6 +61,7 @@ def main():
         rc3, st3, out3, fs3 = run()
         res[name].update({"rc_small": rc2, "status_small": st2, "status_after": st3,
                           "same_after": bool(torch.equal(out3, out) and torch.equal(fs3, fs))})
+    kda.kda_debug_split_segments(0)
     print(json.dumps(res))
 
 

@@ -2,7 +2,8 @@
 path that report KDA_ERR_BOUNDS instead of trapping.
 
 A fresh child process loads the debug library as its only libkda.so.  On a
-dense and a packed batch it must match the fp64 oracle with no check firing;
+dense batch, a packed batch and a dense batch in the segmented form it must
+match the fp64 oracle with no check firing;
 told (through a debug-only hook) that the workspace holds just two chunk
 records, its kernels must report KDA_ERR_BOUNDS without touching memory past
 that point (the real workspace holds every record, so nothing can go astray
@@ -31,7 +32,7 @@ def test_debug_build_checks_fire_and_clean_calls_match():
     assert r.returncode == 0, r.stderr[-3000:]
     res = json.loads(r.stdout.strip().splitlines()[-1])
     assert "debug build" in res["info"]
-    for name in ("dense", "packed"):
+    for name in ("dense", "packed", "segmented"):
         c = res[name]
         assert c["rc"] == 0 and c["status"] == kda.KDA_OK, (name, c)
         assert c["err_o"] <= 1e-2 and c["err_s"] <= 1e-2, (name, c)
