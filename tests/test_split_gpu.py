@@ -306,6 +306,21 @@ def test_host_pipeline_packed_matches_device(lens, s0_std, final):
         np.testing.assert_array_equal(fs.numpy(), s_dev)
 
 
+def test_split_packed_many_short_sequences():
+    """9 000 sequences of 0 to 3 tokens (more than the 8 192 the state CTAs are
+    ordered for, so they run in their own order): every chunk column holds a
+    whole short sequence, empty sequences pass their state through."""
+    rng = np.random.default_rng(5)
+    lens = tuple(int(v) for v in rng.integers(0, 4, size=9000))
+    w = small_workload("pkmany", B=1, T=sum(lens), H=1, dk=128, dv=128, seed=46, varlen=True,
+                       lengths=lens, s0_std=0.03)
+    x = make_inputs(w)
+    o, s = run_packed(x)
+    o_ref, s_ref = oracle.fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["init_state"],
+                              x["cu_seqlens"])
+    assert rel(o, o_ref) <= 1e-2 and rel(s, s_ref) <= 1e-2
+
+
 def test_split_packed_workspace_below_one_column_is_refused():
     lens = (100, 28)
     w = small_workload("pkr", B=1, T=sum(lens), H=2, dk=128, dv=128, seed=44, varlen=True,
