@@ -192,8 +192,9 @@ kda_status kda_decode(const void* q, const void* k, const void* v, const void* g
  * a prefix scan).  Useful when B * H is small against the SM count.
  * workspace: device scratch of kda_seg_workspace_bytes(B, H, nseg, dk, dv)
  * bytes (256-byte aligned), or NULL to take it from the stream-ordered
- * allocator.  nseg = 1 is the plain forward.  kda_chunk_fwd_ex picks a
- * segment count by itself for dense batches that would leave most SMs idle.
+ * allocator.  nseg = 1 is the plain forward.  (kda_chunk_fwd_ex's
+ * automatic path cuts such batches into segments on the two-kernel path;
+ * see its workspace note.)
  */
 kda_status kda_chunk_fwd_seg(const uint16_t* q, const uint16_t* k, const uint16_t* v,
                              const uint16_t* g_logit, const uint16_t* beta,

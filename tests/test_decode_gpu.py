@@ -25,7 +25,7 @@ def rel(a, b):
 
 
 @pytest.mark.parametrize("dtype,tol", [(torch.bfloat16, 1e-2), (torch.float32, 1e-4)])
-@pytest.mark.parametrize("T", [1, 3, 8])
+@pytest.mark.parametrize("T", [1, 3, 8, 16, 37])
 @pytest.mark.parametrize("dk,dv", [(16, 16), (32, 32), (64, 64), (128, 128), (32, 64),
                                    (128, 16)])
 def test_decode_matches_oracle(dtype, tol, T, dk, dv):
