@@ -90,14 +90,19 @@ def alg_flops(w) -> float:
     return per_chunk * th / C
 
 
+# the translation unit of the two-kernel path (less the C header's
+# declarations): the source of the kernels the committed DRAM counters
+# describe, so that edits elsewhere do not make them stale
+SPLIT_SOURCES = ("kda_split.cu", "kda_common.cuh", "sm100.cuh", "kda_tc_util.cuh")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "gated_delta_rule_32_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in SPLIT_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
