@@ -126,8 +126,13 @@ kda_status kda_chunk_fwd_f32(const float* q, const float* k, const float* v,
  *               record per (sequence, head) plus the carried state
  *               (N * H * (66048 + 65536) bytes, rounded up to 256): it then
  *               runs the sequence in more, shorter slices; below that
- *               KDA_ERR_WORKSPACE.  A packed batch needs the full size
- *               (every chunk column, ceil(T / 64) + N at most, at once).
+ *               KDA_ERR_WORKSPACE.  A packed batch runs in slices of
+ *               chunk columns the same way: at least one column's records
+ *               (H * 66048 bytes) after the carried state, the chunk
+ *               offsets, the sequence order and the chunk table
+ *               (kda_workspace_bytes asks for every column's records,
+ *               ceil(T / 64) + N columns at most, while they fit in
+ *               32 GiB).
  *               For a dense batch of few long sequences (6 N H state
  *               CTAs at most one per SM, 384 chunks or more per sequence)
  *               kda_workspace_bytes asks for the records of every chunk
