@@ -72,7 +72,7 @@ typedef enum {
   KDA_ERR_BAD_SEQLENS = 4,  /* cu_seqlens not 0 .. T non-decreasing (device-detected) */
   KDA_ERR_TIMEOUT = 5,      /* a bounded on-chip wait gave up (device-detected) */
   KDA_ERR_CUDA = 6,         /* a CUDA runtime call failed */
-  KDA_ERR_WORKSPACE = 7,    /* workspace given but smaller than kda_workspace_bytes() */
+  KDA_ERR_WORKSPACE = 7,    /* workspace given but below the path's minimum (see kda_chunk_fwd_ex) */
   KDA_ERR_BOUNDS = 8        /* a device-side bounds check failed (KDA_DEBUG builds only) */
 } kda_status;
 
