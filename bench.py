@@ -29,7 +29,7 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from kda_inputs import WORKLOADS, make_inputs, make_unit  # noqa: E402
+from kda_inputs import WORKLOADS, make_inputs, make_unit, small_workload  # noqa: E402
 
 METRIC = "KDA chunked-forward tokens/s at H=32,d=128,T=32K; % of BF16 TC roofline"
 DEFAULT_WORKLOAD = "b2_h32_t32k"
@@ -497,6 +497,59 @@ def run_ours(args):
     return 0
 
 
+def run_decode(args):
+    """The decode / rebuild kernel alone (one GPU): T tokens per call for B x H
+    states of d = 128, bf16 inputs; one JSON line with tokens/s and the
+    fraction of the measured HBM bandwidth its state and input bytes take."""
+    from gated_delta_rule_32_gb300 import build as kbuild
+    from gated_delta_rule_32_gb300 import kda
+
+    B, H, T = args.B or 64, args.H or 32, args.decode
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    dev = torch.device("cuda:0")
+    kbuild.build()
+    kda.load()
+    w = small_workload("decode", B=B, T=T, H=H, dk=128, dv=128, s0_std=0.02, seed=9)
+    x = make_inputs(w)
+    d = {k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in x.items()}
+    state = d["init_state"].clone()
+    out = torch.empty_like(d["v"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        rc = kda.kda_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], state, out, B, T, H, 128,
+                            128, kda.KDA_BF16, 1.0, stream)
+        if rc != 0:
+            raise RuntimeError("kda_decode: " + kda.status_string(rc))
+    for _ in range(args.warmup):
+        step()
+    steps = args.steps or 200
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = B * H * 128 * 128 * 4 * 2 + B * T * H * (4 * 128 + 1) * 2 + B * T * H * 128 * 2
+    hbm_gbs, _, peak_src = measured_peaks()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    print(json.dumps({"metric": "KDA decode tokens/s (state in registers, %d tokens per call)" % T,
+                      "value": B * T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
+                      "steps": steps, "warmup": args.warmup, "ms_per_step": ms,
+                      "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                      "config": {"workload": "decode", "B": B, "H": H, "T": T, "dk": 128,
+                                 "dv": 128},
+                      "gpu_launches": steps,
+                      "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs,
+                                   "unit": "GB/s", "frac": achieved / hbm_gbs,
+                                   "traffic": None, "alg_bytes_per_launch": nbytes,
+                                   "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)"}}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -518,9 +571,14 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=32768)
     ap.add_argument("--ref-units", type=int, default=16)
     ap.add_argument("--ref-tokens", type=int, default=4096)
+    ap.add_argument("--decode", type=int, default=0, metavar="TOKENS",
+                    help="instead of the forward: the decode kernel on --B x --H states "
+                         "(default 64 x 32, d = 128) for TOKENS tokens per call")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
+    if args.decode:
+        return run_decode(args)
     if args.impl == "reference":
         if not args.steps:
             args.steps = 5
