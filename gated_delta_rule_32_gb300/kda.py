@@ -246,6 +246,9 @@ def forward(q, k, v, g_logit, beta, init_state=None, cu_seqlens=None, scale=1.0,
     q, k, g_logit [B,T,H,dk], v [B,T,H,dv], beta [B,T,H] CUDA tensors of one
     dtype (bfloat16 or float32); init_state [N,H,dk,dv] fp32 or None;
     cu_seqlens int32 [N+1] CUDA tensor or None.  Returns (out, final_state).
+    The workspace comes from PyTorch's caching allocator (a block it keeps
+    and hands out again on the next call), not from the library's own
+    stream-ordered allocation.
     """
     import torch
     B, T, H, dk = q.shape
@@ -257,8 +260,13 @@ def forward(q, k, v, g_logit, beta, init_state=None, cu_seqlens=None, scale=1.0,
         if output_final_state else None
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
+    nb = kda_workspace_bytes(N, T, H, dk, dv, dtype, chunk_size, algo,
+                             int(cu_seqlens is not None))
+    ws = torch.empty(nb, dtype=torch.uint8, device=q.device) if nb else None
+    if ws is not None and isinstance(stream, torch.cuda.Stream):
+        ws.record_stream(stream)  # (freed for reuse only after the work on `stream`)
     rc = kda_chunk_fwd_ex(q, k, v, g_logit, beta, init_state, out, fs, N, T, H, dk, dv,
-                          cu_seqlens, dtype, chunk_size, scale, algo, None, 0, dev_status,
+                          cu_seqlens, dtype, chunk_size, scale, algo, ws, nb, dev_status,
                           stream)
     if rc != KDA_OK:
         raise KdaError("kda_chunk_fwd_ex", rc)
